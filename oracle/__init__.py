@@ -1,0 +1,173 @@
+"""CPU oracle for query-aware page selection + masked sparse attention (fp64).
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, the smoke check and the
+benchmark's CPU-baseline leg, never by the library.  The arithmetic lives in
+``oracle.c`` (plain C, fp64); this module only compiles it with gcc, loads it
+with ctypes and marshals numpy arrays.  It shares no code with the CUDA path.
+
+All functions work on logical token order for ONE (sequence, KV head) unless
+stated otherwise; inputs are widened to float64 before the call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc, -O2, no CUDA)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp,
+                               _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_page_bounds.argtypes = [ctypes.c_int] * 3 + [_D, _D, _D]
+            lib.oracle_page_bounds_by_appends.argtypes = [ctypes.c_int] * 3 + [
+                _D, ctypes.c_int, _I, _D, _D]
+            lib.oracle_page_scores.argtypes = [ctypes.c_int] * 3 + [_D, _D, _D, _D]
+            lib.oracle_select_pages.argtypes = [ctypes.c_int, _D, ctypes.c_int, _I]
+            lib.oracle_select_pages.restype = ctypes.c_int
+            lib.oracle_attention.argtypes = [ctypes.c_int] * 4 + [
+                _D, _D, _D, ctypes.c_int, _I, ctypes.c_double, _D]
+            lib.oracle_decode_unit.argtypes = [ctypes.c_int] * 4 + [
+                _D, _D, _D, _D, _D, ctypes.c_int, ctypes.c_double, _D, _I, _D]
+            lib.oracle_decode_unit.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i32(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _dp(a: np.ndarray):
+    return a.ctypes.data_as(_D)
+
+
+def _ip(a: np.ndarray):
+    return a.ctypes.data_as(_I)
+
+
+def num_pages(L: int, P: int) -> int:
+    return (int(L) + int(P) - 1) // int(P)
+
+
+def page_bounds(K, P: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-page per-channel (min, max) of the keys K [L, d]; returns lo, hi [N, d]."""
+    K = _f64(K)
+    L, d = K.shape
+    N = num_pages(L, P)
+    lo = np.empty((N, d))
+    hi = np.empty((N, d))
+    if N:
+        _load().oracle_page_bounds(L, d, P, _dp(K), _dp(lo), _dp(hi))
+    return lo, hi
+
+
+def page_bounds_by_appends(K, P: int, chunk_lens: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
+    """Boxes maintained chunk by chunk as an append-time builder would."""
+    K = _f64(K)
+    L, d = K.shape
+    N = num_pages(L, P)
+    lo = np.full((N, d), np.nan)
+    hi = np.full((N, d), np.nan)
+    ch = _i32(chunk_lens)
+    if N:
+        _load().oracle_page_bounds_by_appends(L, d, P, _dp(K), len(ch), _ip(ch), _dp(lo), _dp(hi))
+    return lo, hi
+
+
+def page_scores(q, lo, hi) -> np.ndarray:
+    """Score of every page: max_g sum_c max(q[g,c]*lo[p,c], q[g,c]*hi[p,c])."""
+    q, lo, hi = _f64(q), _f64(lo), _f64(hi)
+    if q.ndim == 1:
+        q = q[None]
+    G, d = q.shape
+    N = lo.shape[0]
+    s = np.empty(N)
+    if N:
+        _load().oracle_page_scores(G, d, N, _dp(q), _dp(lo), _dp(hi), _dp(s))
+    return s
+
+
+def select_pages(scores, k: int) -> np.ndarray:
+    """Kept logical page ids (ascending) for a budget of k pages."""
+    s = _f64(scores)
+    N = s.shape[0]
+    out = np.empty(max(N, 1), dtype=np.int32)
+    n = _load().oracle_select_pages(N, _dp(s), int(k), _ip(out))
+    return out[:n].copy()
+
+
+def attention(q, K, V, L: int, P: int, pages, scale: Optional[float] = None) -> np.ndarray:
+    """Masked softmax attention of q [G, d] over the tokens of ``pages`` below L."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    if q.ndim == 1:
+        q = q[None]
+    G, d = q.shape
+    pg = _i32(pages)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.empty((G, d))
+    _load().oracle_attention(G, d, int(L), int(P), _dp(q), _dp(K), _dp(V), len(pg),
+                             _ip(pg if len(pg) else np.zeros(1, np.int32)), float(scale),
+                             _dp(out))
+    return out
+
+
+def dense_attention(q, K, V, L: int, P: int, scale: Optional[float] = None) -> np.ndarray:
+    return attention(q, K, V, L, P, np.arange(num_pages(L, P)), scale)
+
+
+def decode_unit(q, K, V, lo, hi, L: int, P: int, k: int, scale: Optional[float] = None):
+    """One decode step of one (sequence, KV head): scores, kept ids, output [G, d]."""
+    q, K, V, lo, hi = _f64(q), _f64(K), _f64(V), _f64(lo), _f64(hi)
+    if q.ndim == 1:
+        q = q[None]
+    G, d = q.shape
+    N = num_pages(L, P)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    scores = np.empty(max(N, 1))
+    sel = np.empty(max(N, 1), dtype=np.int32)
+    out = np.empty((G, d))
+    n = _load().oracle_decode_unit(G, d, int(L), int(P), _dp(q), _dp(K), _dp(V), _dp(lo),
+                                   _dp(hi), int(k), float(scale), _dp(scores), _ip(sel),
+                                   _dp(out))
+    return scores[:N].copy(), sel[:n].copy(), out
+
+
+def run_units(fn, items, threads: int = 1):
+    """Map ``fn`` over independent (sequence, KV head) units; ctypes drops the GIL
+    during each C call, so threads run the C code in parallel."""
+    if threads <= 1:
+        return [fn(it) for it in items]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, items))

@@ -1,0 +1,204 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU statement of query-aware page selection
+ * followed by masked attention over the selected pages.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path links,
+ * loads or calls this file; only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code, header, table or helper
+ * with the CUDA path.
+ *
+ * Source of the method: "TinyServe: Query-Aware Cache Selection for Efficient
+ * LLM Serving" (arXiv 2509.12211), section 方法详解 / 关键设计: every KV-cache
+ * block carries a bounding box of what it contains; at decode time the query
+ * is compared with every block's box and the blocks with the highest
+ * similarity are loaded; the abstract adds that scoring, sparse memory access
+ * and masked attention form one decode step.  The pages give no formula; the
+ * readings used here are:
+ *   - the box of page p is the per-channel minimum lo[p][c] and maximum
+ *     hi[p][c] of the keys stored in its valid slots;
+ *   - the similarity is the largest value q.k can take inside the box,
+ *     sum_c max(q_c*lo_c, q_c*hi_c), maximised over the query heads that share
+ *     the KV head (grouped-query attention);
+ *   - the sink page (logical page 0) and the newest page (N-1) are always
+ *     kept; the remaining budget goes to the highest scores, ties to the lower
+ *     page index; a budget of at least N keeps every page;
+ *   - attention is softmax(scale * q.k) over the tokens of the kept pages whose
+ *     position is below the sequence length, times V, with scale = 1/sqrt(d).
+ *
+ * Every function works on ONE (sequence, KV head) with logical (not physical)
+ * token order: K and V are [L][d] row-major, q is [G][d].  All arithmetic is
+ * fp64.  No blocking, no fusion, no reordering beyond the definitions.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+static int num_pages_of(int L, int P) { return (L + P - 1) / P; }
+
+/* Bounding box of every page, computed from scratch over its valid tokens.
+ * lo, hi: [N][d] with N = ceil(L/P). */
+void oracle_page_bounds(int L, int d, int P, const double *K, double *lo, double *hi)
+{
+    int N = num_pages_of(L, P);
+    for (int p = 0; p < N; ++p) {
+        int t0 = p * P, t1 = (p + 1) * P < L ? (p + 1) * P : L;
+        for (int c = 0; c < d; ++c) {
+            double mn = K[(size_t)t0 * d + c], mx = mn;
+            for (int t = t0 + 1; t < t1; ++t) {
+                double x = K[(size_t)t * d + c];
+                if (x < mn) mn = x;
+                if (x > mx) mx = x;
+            }
+            lo[(size_t)p * d + c] = mn;
+            hi[(size_t)p * d + c] = mx;
+        }
+    }
+}
+
+/* The same boxes, maintained the way an append-time builder keeps them:
+ * tokens arrive in chunks (chunk_lens sums to L); each chunk writes its tokens
+ * into their slots and folds them into the box of their page; a page whose
+ * slot 0 is written by the chunk starts a fresh box.  Independent of
+ * oracle_page_bounds so the two can pin each other. */
+void oracle_page_bounds_by_appends(int L, int d, int P, const double *K, int n_chunks,
+                                   const int *chunk_lens, double *lo, double *hi)
+{
+    int pos = 0;
+    for (int ch = 0; ch < n_chunks; ++ch) {
+        for (int i = 0; i < chunk_lens[ch]; ++i, ++pos) {
+            if (pos >= L) return;
+            int p = pos / P, slot = pos % P;
+            const double *k = K + (size_t)pos * d;
+            double *l = lo + (size_t)p * d, *h = hi + (size_t)p * d;
+            for (int c = 0; c < d; ++c) {
+                if (slot == 0) {
+                    l[c] = k[c];
+                    h[c] = k[c];
+                } else {
+                    l[c] = fmin(l[c], k[c]);
+                    h[c] = fmax(h[c], k[c]);
+                }
+            }
+        }
+    }
+}
+
+/* Score of every page: max over the G query heads of the largest q.k inside
+ * the page's box.  s: [N]. */
+void oracle_page_scores(int G, int d, int N, const double *q, const double *lo,
+                        const double *hi, double *s)
+{
+    for (int p = 0; p < N; ++p) {
+        double best = -INFINITY;
+        for (int g = 0; g < G; ++g) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) {
+                double a = q[(size_t)g * d + c] * lo[(size_t)p * d + c];
+                double b = q[(size_t)g * d + c] * hi[(size_t)p * d + c];
+                acc += a > b ? a : b;
+            }
+            if (acc > best) best = acc;
+        }
+        s[p] = best;
+    }
+}
+
+/* Ranking used by the selection: higher score first, equal scores by lower
+ * page index; a NaN score ranks after every number. */
+static _Thread_local const double *g_rank_scores;  /* per thread: callers may run units in parallel */
+static int rank_cmp(const void *pa, const void *pb)
+{
+    int a = *(const int *)pa, b = *(const int *)pb;
+    double sa = g_rank_scores[a], sb = g_rank_scores[b];
+    int na = isnan(sa), nb = isnan(sb);
+    if (na != nb) return na ? 1 : -1;
+    if (!na && sa != sb) return sa > sb ? -1 : 1;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+static int int_cmp(const void *pa, const void *pb)
+{
+    int a = *(const int *)pa, b = *(const int *)pb;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+/* Pages kept for a budget of k pages, ascending logical ids, written to sel
+ * (room for N ids).  Returns how many were kept:
+ *   k >= N        -> all N pages;
+ *   otherwise     -> the forced pages {0, N-1} plus the best k - |forced|
+ *                    others (at least the forced pages, whatever k is). */
+int oracle_select_pages(int N, const double *s, int k, int *sel)
+{
+    if (N <= 0) return 0;
+    if (k >= N) {
+        for (int p = 0; p < N; ++p) sel[p] = p;
+        return N;
+    }
+    int nforced = N >= 2 ? 2 : 1;
+    int take = k - nforced;
+    if (take < 0) take = 0;
+    int ncand = N - nforced;
+    int *cand = (int *)malloc(sizeof(int) * (ncand > 0 ? ncand : 1));
+    for (int i = 0; i < ncand; ++i) cand[i] = i + 1;  /* pages 1 .. N-2 */
+    g_rank_scores = s;
+    qsort(cand, (size_t)ncand, sizeof(int), rank_cmp);
+    int n = 0;
+    sel[n++] = 0;
+    if (N >= 2) sel[n++] = N - 1;
+    for (int i = 0; i < take && i < ncand; ++i) sel[n++] = cand[i];
+    free(cand);
+    qsort(sel, (size_t)n, sizeof(int), int_cmp);
+    return n;
+}
+
+/* Masked softmax attention of G query heads over the tokens of the listed
+ * pages with position < L.  out: [G][d].  Two passes (max, then exponentials)
+ * as in the textbook definition.  An empty token set gives zeros. */
+void oracle_attention(int G, int d, int L, int P, const double *q, const double *K,
+                      const double *V, int npages, const int *pages, double scale,
+                      double *out)
+{
+    for (int g = 0; g < G; ++g) {
+        const double *qg = q + (size_t)g * d;
+        double *og = out + (size_t)g * d;
+        double m = -INFINITY;
+        for (int i = 0; i < npages; ++i) {
+            for (int t = pages[i] * P; t < (pages[i] + 1) * P && t < L; ++t) {
+                double z = 0.0;
+                for (int c = 0; c < d; ++c) z += qg[c] * K[(size_t)t * d + c];
+                z *= scale;
+                if (z > m) m = z;
+            }
+        }
+        for (int c = 0; c < d; ++c) og[c] = 0.0;
+        if (m == -INFINITY) continue;
+        double denom = 0.0;
+        for (int i = 0; i < npages; ++i) {
+            for (int t = pages[i] * P; t < (pages[i] + 1) * P && t < L; ++t) {
+                double z = 0.0;
+                for (int c = 0; c < d; ++c) z += qg[c] * K[(size_t)t * d + c];
+                double w = exp(z * scale - m);
+                denom += w;
+                for (int c = 0; c < d; ++c) og[c] += w * V[(size_t)t * d + c];
+            }
+        }
+        for (int c = 0; c < d; ++c) og[c] /= denom;
+    }
+}
+
+/* One decode step of one (sequence, KV head), from boxes already maintained:
+ * score every page, keep the budget, attend over the kept pages.
+ * sel must hold N ids; returns how many pages were kept. */
+int oracle_decode_unit(int G, int d, int L, int P, const double *q, const double *K,
+                       const double *V, const double *lo, const double *hi, int k,
+                       double scale, double *scores, int *sel, double *out)
+{
+    int N = num_pages_of(L, P);
+    if (N <= 0) {
+        for (int i = 0; i < G * d; ++i) out[i] = 0.0;
+        return 0;
+    }
+    oracle_page_scores(G, d, N, q, lo, hi, scores);
+    int n = oracle_select_pages(N, scores, k, sel);
+    oracle_attention(G, d, L, P, q, K, V, n, sel, scale, out);
+    return n;
+}

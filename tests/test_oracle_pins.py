@@ -1,0 +1,250 @@
+"""Pins of the CPU oracle against facts fixed outside it (no GPU).
+
+The pages print no worked example, so every pin is a closed form, an
+invariant, a brute-force enumeration on tiny inputs, or a reduction to a
+library routine (numpy min/max, a matmul, scipy's softmax).  Each is chosen so
+that a plausible slip in the oracle -- a swapped lo/hi, a dropped head in the
+group maximum, an off-by-one page range, an inverted tie rule, a missing
+softmax scale or mask -- fails at least one of them.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------- page boxes
+
+@pytest.mark.parametrize("L,P", [(1, 16), (16, 16), (37, 16), (100, 32), (64, 8)])
+def test_bounds_equal_numpy_minmax(L, P):
+    K = rng(L).standard_normal((L, 12))
+    lo, hi = oracle.page_bounds(K, P)
+    N = -(-L // P)
+    assert lo.shape == (N, 12)
+    for p in range(N):
+        rows = K[p * P:min((p + 1) * P, L)]
+        assert np.array_equal(lo[p], rows.min(axis=0))
+        assert np.array_equal(hi[p], rows.max(axis=0))
+
+
+@pytest.mark.parametrize("chunks", [[1] * 50, [7, 9, 1, 33], [16, 16, 18], [50], [3, 13, 2, 2, 30]])
+def test_bounds_by_appends_equal_from_scratch(chunks):
+    L = sum(chunks)
+    K = rng(L).standard_normal((L, 8))
+    a = oracle.page_bounds(K, 16)
+    b = oracle.page_bounds_by_appends(K, 16, chunks)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------- scores
+
+def _brute_max_qk(q, K, L, P):
+    N = -(-L // P)
+    out = np.empty(N)
+    for p in range(N):
+        rows = K[p * P:min((p + 1) * P, L)]
+        out[p] = np.max(q @ rows.T)
+    return out
+
+
+@pytest.mark.parametrize("G,d,L,P", [(1, 16, 70, 16), (4, 32, 129, 16), (8, 64, 256, 32)])
+def test_score_upper_bounds_every_true_logit(G, d, L, P):
+    r = rng(G * 1000 + d)
+    q = r.standard_normal((G, d))
+    K = r.standard_normal((L, d)) * r.lognormal(0, 0.5, size=d)
+    lo, hi = oracle.page_bounds(K, P)
+    s = oracle.page_scores(q, lo, hi)
+    true = _brute_max_qk(q, K, L, P)
+    assert np.all(s >= true - 1e-12 * np.abs(true).max())
+
+
+@pytest.mark.parametrize("G", [1, 3, 8])
+def test_score_tight_when_all_keys_equal(G):
+    r = rng(G)
+    d, P = 48, 16
+    q = r.standard_normal((G, d))
+    K = r.standard_normal((4 * P, d))
+    K[P:2 * P] = K[P]                       # page 1: every key identical
+    lo, hi = oracle.page_bounds(K, P)
+    s = oracle.page_scores(q, lo, hi)
+    expect = max(float(np.dot(q[g], K[P])) for g in range(G))
+    assert s[1] == pytest.approx(expect, rel=1e-13, abs=1e-13)
+
+
+def test_score_equals_sign_split_matmul():
+    # sum_c max(q lo, q hi) == q+ . hi + q- . lo when lo <= hi (a different formula)
+    r = rng(7)
+    G, d, N = 8, 64, 40
+    q = r.standard_normal((G, d))
+    a, b = r.standard_normal((N, d)), r.standard_normal((N, d))
+    lo, hi = np.minimum(a, b), np.maximum(a, b)
+    qp, qm = np.maximum(q, 0), np.minimum(q, 0)
+    expect = (qp @ hi.T + qm @ lo.T).max(axis=0)
+    assert np.allclose(oracle.page_scores(q, lo, hi), expect, rtol=1e-13, atol=1e-13)
+
+
+def test_score_orientation_closed_form():
+    lo = np.array([[-1.0, 0.0]])
+    hi = np.array([[2.0, 0.0]])
+    assert oracle.page_scores(np.array([1.0, 0.0]), lo, hi)[0] == 2.0
+    assert oracle.page_scores(np.array([-1.0, 0.0]), lo, hi)[0] == 1.0
+    # group maximum, not sum or mean, over the heads sharing the KV head
+    q = np.array([[1.0, 0.0], [-3.0, 0.0]])
+    assert oracle.page_scores(q, lo, hi)[0] == 3.0
+
+
+def test_score_negative_group_max_is_not_clamped_at_zero():
+    lo = np.array([[1.0, 1.0]])
+    hi = np.array([[2.0, 2.0]])
+    q = np.array([[-1.0, -1.0], [-2.0, -0.5]])
+    assert oracle.page_scores(q, lo, hi)[0] == -2.0
+
+
+# ---------------------------------------------------------------- selection
+
+def _brute_select(s, k):
+    N = len(s)
+    if k >= N:
+        return list(range(N))
+    forced = [0, N - 1] if N >= 2 else [0]
+    cand = [p for p in range(N) if p not in forced]
+    take = max(k - len(forced), 0)
+    best = None
+    for sub in itertools.combinations(cand, take):
+        tot = sum(s[p] for p in sub)
+        key = (-tot, tuple(sorted(sub)))
+        if best is None or key < best[0]:
+            best = (key, sub)
+    return sorted(forced + list(best[1]))
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 11])
+def test_select_matches_bruteforce_with_ties(N):
+    r = rng(N)
+    for trial in range(6):
+        s = r.integers(-3, 4, size=N).astype(np.float64)   # many exact ties
+        for k in range(1, N + 2):
+            got = oracle.select_pages(s, k).tolist()
+            assert got == _brute_select(s.tolist(), k), (s, k)
+
+
+def test_select_ties_go_to_lower_index():
+    s = np.zeros(10)
+    assert oracle.select_pages(s, 5).tolist() == [0, 1, 2, 3, 9]
+    s[7] = 1.0
+    assert oracle.select_pages(s, 4).tolist() == [0, 1, 7, 9]
+
+
+def test_select_forced_pages_and_budget_floor():
+    s = np.arange(10, dtype=np.float64)[::-1].copy()  # page 0 best, page 9 worst
+    s[0], s[9] = -100.0, -100.0
+    assert oracle.select_pages(s, 1).tolist() == [0, 9]      # forced even over budget
+    assert oracle.select_pages(s, 3).tolist() == [0, 1, 9]
+    assert oracle.select_pages(np.array([5.0]), 1).tolist() == [0]
+    assert oracle.select_pages(np.array([5.0, 1.0]), 1).tolist() == [0, 1]
+    assert oracle.select_pages(s, 10).tolist() == list(range(10))
+    assert oracle.select_pages(s, 99).tolist() == list(range(10))
+
+
+def test_select_nan_ranks_last():
+    s = np.array([0.0, np.nan, 1.0, np.nan, 0.5, 0.0])
+    assert oracle.select_pages(s, 3).tolist() == [0, 2, 5]
+
+
+# ---------------------------------------------------------------- attention
+
+def _textbook(q, K, V, L, scale):
+    z = scale * (q @ K[:L].T)
+    return scipy.special.softmax(z, axis=-1) @ V[:L]
+
+
+@pytest.mark.parametrize("G,d,L,P", [(1, 8, 1, 16), (2, 16, 33, 16), (8, 64, 300, 32)])
+def test_dense_attention_equals_scipy_softmax(G, d, L, P):
+    r = rng(L)
+    q, K, V = r.standard_normal((G, d)), r.standard_normal((L + 5, d)), r.standard_normal((L + 5, d))
+    got = oracle.dense_attention(q, K, V, L, P)
+    assert np.allclose(got, _textbook(q, K, V, L, 1 / math.sqrt(d)), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_over_pages_equals_dense_over_their_tokens():
+    r = rng(11)
+    G, d, P, L = 4, 16, 16, 150
+    q, K, V = r.standard_normal((G, d)), r.standard_normal((L, d)), r.standard_normal((L, d))
+    pages = [0, 3, 5, 9]                              # 9 is the partial newest page
+    toks = np.concatenate([np.arange(p * P, min((p + 1) * P, L)) for p in pages])
+    got = oracle.attention(q, K, V, L, P, pages)
+    expect = _textbook(q, K[toks], V[toks], len(toks), 1 / math.sqrt(d))
+    assert np.allclose(got, expect, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_single_token_returns_v():
+    r = rng(3)
+    q, K, V = r.standard_normal((3, 8)), r.standard_normal((1, 8)), r.standard_normal((1, 8))
+    assert np.allclose(oracle.dense_attention(q, K, V, 1, 16), np.repeat(V, 3, 0), rtol=0, atol=1e-15)
+
+
+def test_attention_equal_logits_give_mean_of_valid_values():
+    r = rng(4)
+    K, V = r.standard_normal((40, 8)), r.standard_normal((40, 8))
+    out = oracle.dense_attention(np.zeros((2, 8)), K, V, 37, 16)
+    assert np.allclose(out, V[:37].mean(axis=0)[None], rtol=1e-13, atol=1e-14)
+
+
+def test_attention_ignores_tokens_at_or_beyond_length():
+    r = rng(5)
+    q, K, V = r.standard_normal((2, 8)), r.standard_normal((48, 8)), r.standard_normal((48, 8))
+    a = oracle.dense_attention(q, K, V, 37, 16)
+    K2, V2 = K.copy(), V.copy()
+    K2[37:] = 1e3
+    V2[37:] = -1e3
+    assert np.array_equal(a, oracle.dense_attention(q, K2, V2, 37, 16))
+
+
+def test_attention_scale_is_inverse_sqrt_d():
+    # two tokens, logits differ by 1 before scaling: weights are sigmoid(+-1/sqrt(d))
+    d = 16
+    q = np.zeros((1, d)); q[0, 0] = 1.0
+    K = np.zeros((2, d)); K[1, 0] = 1.0
+    V = np.zeros((2, d)); V[1, 1] = 1.0
+    out = oracle.dense_attention(q, K, V, 2, 16)
+    assert out[0, 1] == pytest.approx(1 / (1 + math.exp(-1 / math.sqrt(d))), rel=1e-14)
+
+
+# --------------------------------------------------- full step (decode unit)
+
+def test_full_budget_equals_dense():
+    r = rng(12)
+    G, d, P, L = 4, 32, 16, 200
+    q, K, V = r.standard_normal((G, d)), r.standard_normal((L, d)), r.standard_normal((L, d))
+    lo, hi = oracle.page_bounds(K, P)
+    N = -(-L // P)
+    dense = oracle.dense_attention(q, K, V, L, P)
+    for k in (N, N + 5):
+        s, sel, out = oracle.decode_unit(q, K, V, lo, hi, L, P, k)
+        assert sel.tolist() == list(range(N))
+        assert np.array_equal(out, dense)
+
+
+def test_decode_unit_composes_the_three_steps():
+    r = rng(13)
+    G, d, P, L, k = 2, 16, 16, 333, 6
+    q, K, V = r.standard_normal((G, d)), r.standard_normal((L, d)), r.standard_normal((L, d))
+    lo, hi = oracle.page_bounds(K, P)
+    s, sel, out = oracle.decode_unit(q, K, V, lo, hi, L, P, k)
+    assert np.array_equal(s, oracle.page_scores(q, lo, hi))
+    assert np.array_equal(sel, oracle.select_pages(s, k))
+    assert np.array_equal(out, oracle.attention(q, K, V, L, P, sel))
+
+
+def test_empty_sequence_gives_zeros():
+    s, sel, out = oracle.decode_unit(np.ones((2, 4)), np.zeros((0, 4)), np.zeros((0, 4)),
+                                     np.zeros((0, 4)), np.zeros((0, 4)), 0, 16, 4)
+    assert len(sel) == 0 and np.all(out == 0)
