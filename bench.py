@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: query-aware sparse paged attention on GB300.
+
+One step = one decode step of one attention layer for the whole batch: score
+every page of every (sequence, KV head) against its bounding box, keep the
+budget, attend over the kept pages (two kernels, chained with programmatic
+dependent launch).  Inputs are resident in HBM before the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are weak scaling:
+every rank decodes its own batch (seed offset by rank); no data-path
+collective exists.  --impl reference times the CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode queries/sec and HBM GB/s (% roofline) at 8K ctx, 12.5% budget"
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attention_headline_8k.md")
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank decodes its own batch: weak scaling, no shared data."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------ accounting
+
+def algorithmic_bytes(cfg, lens, budgets):
+    """Bytes the method must move per step (and per kernel), per (sequence, KV head):
+    select:    N_b*2*d*es (page boxes) + G*d*es (q) + 4*N_b (block table) + 4*k_b (ids out)
+    attention: k_b*2*P*d*es (kept K and V page tiles) + 2*G*d*es (q, out) + 8*k_b (ids, table)
+    """
+    es = 4 if cfg.dtype == "f32" else 2
+    d, P, G, Hkv = cfg.head_dim, cfg.page_size, cfg.group, cfg.num_kv_heads
+    N = (np.asarray(lens, np.int64) + P - 1) // P
+    k = np.minimum(N, np.maximum(np.asarray(budgets, np.int64), np.minimum(N, 2)))
+    sel = Hkv * (N * 2 * d * es + G * d * es + 4 * N + 4 * k)
+    att = Hkv * (k * 2 * P * d * es + 2 * G * d * es + 8 * k)
+    dense = Hkv * (N * 2 * P * d * es + 2 * G * d * es + 4 * N)
+    return int(sel.sum()), int(att.sum()), int(dense.sum())
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("attention.cu", "qasa_device.cuh", "qasa_launch.h"):
+        with open(os.path.join(ROOT, "query_aware_sparse_append_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            text = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("bench-key "):
+            k, _, v = line[len("bench-key "):].partition("=")
+            vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != kernel_source_digest():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[2:6]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(cfg, seed, seconds=15.0, threads=None):
+    """Time the CPU oracle (as it stands) on (sequence, KV head) units of the
+    workload until `seconds` of work are done; returns queries/s and details.
+    Page boxes are built outside the timing, as the GPU path keeps them at
+    append time; the timed part is score + select + attend per unit."""
+    import oracle
+    from query_aware_sparse_append_gb300 import workloads as W
+    threads = threads or os.cpu_count() or 1
+    oracle.build()
+    lens = W.seq_lens(cfg, seed)
+    bud = W.budgets(cfg, lens)
+    scales = W.key_channel_scales(cfg, seed)
+    G, P = cfg.group, cfg.page_size
+    units = []
+    b = 0
+    t_prep = time.time()
+    while b < cfg.batch and (len(units) < 4 * threads or time.time() - t_prep < 5):
+        s = W.sequence(cfg, b, int(lens[b]), seed, scales)
+        for h in range(cfg.num_kv_heads):
+            K = W.widen(s.k[:, h], cfg.dtype)
+            V = W.widen(s.v[:, h], cfg.dtype)
+            q = W.widen(s.q[h * G:(h + 1) * G], cfg.dtype)
+            lo, hi = oracle.page_bounds(K, P)
+            units.append((q, K, V, lo, hi, int(lens[b]), int(bud[b])))
+        b += 1
+
+    def one(u):
+        q, K, V, lo, hi, L, k = u
+        oracle.decode_unit(q, K, V, lo, hi, L, P, k)
+        return 1
+
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.run_units(one, units, threads=threads)
+        done += len(units)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    qps = done / cfg.num_kv_heads / el
+    return {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
+            "sample": "%d (sequence, KV head) units of %s (%d sequences) repeated for %.1f s; "
+                      "score+select+attend per unit, fp64, page boxes prebuilt"
+                      % (done, cfg.name, b, el)}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from query_aware_sparse_append_gb300 import workloads as W
+    cfg = W.CONFIGS[args.config]
+    per_step = max(2.0, 30.0 / max(1, args.steps + args.warmup))
+    base = oracle_sample(cfg, args.seed, seconds=per_step * (args.steps + args.warmup))
+    v = base["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * cfg.batch / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(cfg), "cpu_baseline": base,
+            "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(cfg):
+    return {"workload": cfg.name, "batch": cfg.batch, "ctx": [cfg.ctx_min, cfg.ctx_max],
+            "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
+            "head_dim": cfg.head_dim, "page_size": cfg.page_size,
+            "budget": ("%g%% of pages" % (cfg.budget_value / 10.0)
+                       if cfg.budget_kind == "permille" else "%d pages" % cfg.budget_value),
+            "kv_dtype": cfg.dtype, "physical_pages": "shuffled",
+            "l2": "256 MB write between timed steps; per-step bytes also exceed L2"}
+
+
+# ------------------------------------------------------------ GPU leg
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    from query_aware_sparse_append_gb300 import build
+    build.build()
+    from query_aware_sparse_append_gb300 import binding as qasa
+    from query_aware_sparse_append_gb300 import paged
+    from query_aware_sparse_append_gb300 import workloads as W
+
+    cfg = W.CONFIGS[args.config]
+    seed = rank_seed(args.seed, rank)
+    wl = paged.load(paged.generate(cfg, seed=seed), device=dev)
+    B, Hq, Hkv, d = cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
+    maxp = wl.block_table.shape[1]
+    max_budget = wl.max_budget
+    ws = qasa.alloc_workspace(wl.cache, B, Hq, maxp, device=dev)
+    out = torch.empty_like(wl.q_dev)
+    sel = torch.empty((B, Hkv, max_budget), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        qasa.sparse_decode_attention(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev,
+                                     wl.budget_dev, max_budget=max_budget, out=out,
+                                     selected=sel, workspace=ws, status=status)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K fused decode steps, L2 flushed before each
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    ms_all = max_over_ranks(ms, dev)
+    st = int(status.item())
+    if st:
+        raise SystemExit("device errors during the benchmark: %s" % qasa.decode_device_errors(st))
+
+    # ---- per-kernel breakdown (same inputs, the two kernels as separate calls)
+    ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev3[i][0].record(stream)
+        qasa.select_pages(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev, wl.budget_dev,
+                          max_budget, selected=sel, workspace=ws, status=status)
+        ev3[i][1].record(stream)
+        qasa.sparse_attention(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev, wl.budget_dev, sel,
+                              out=out, workspace=ws, status=status)
+        ev3[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    sel_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev3)
+    att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev3)
+
+    # ---- dense path (every page), for comparison
+    dense_out = torch.empty_like(out)
+    evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(max(3, args.steps // 2))]
+    for a, b_ in evd:
+        flush.zero_()
+        a.record(stream)
+        qasa.dense_decode_attention(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev,
+                                    out=dense_out, workspace=ws, status=status)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    dense_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in evd)
+
+    # ---- end to end through the public API with pinned host buffers
+    q_h = wl.q_dev.cpu().pin_memory()
+    lens_h = wl.lens_dev.cpu().pin_memory()
+    bud_h = wl.budget_dev.cpu().pin_memory()
+    bt_h = wl.block_table.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    sel_h = torch.empty(sel.shape, dtype=sel.dtype).pin_memory()
+    q_d, lens_d, bud_d, bt_d = (torch.empty_like(x, device=dev) for x in (q_h, lens_h, bud_h, bt_h))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        bud_d.copy_(bud_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        qasa.sparse_decode_attention(wl.cache, q_d, bt_d, lens_d, bud_d, max_budget=max_budget,
+                                     out=out, selected=sel, workspace=ws, status=status)
+        out_h.copy_(out, non_blocking=True)
+        sel_h.copy_(sel, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_ms.append(1000.0 * (time.perf_counter() - t0))
+    e2e_mean = max_over_ranks(statistics.mean(e2e_ms), dev)
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, lens_h, bud_h, bt_h))
+    d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
+
+    if rank != 0:
+        return 0
+    sel_b, att_b, dense_b = algorithmic_bytes(cfg, wl.lens, wl.budgets)
+    peak, peak_kind = measured_peak()
+    att_gbs = att_b / (att_ms * 1e-3) / 1e9
+    step_gbs = (sel_b + att_b) / (ms * 1e-3) / 1e9
+    cpu = oracle_sample(cfg, seed, seconds=args.cpu_seconds) if args.cpu_seconds > 0 else None
+    line = {
+        "metric": METRIC,
+        "value": world * B / (ms_all * 1e-3),
+        "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_all,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic",
+        "config": config_block(cfg),
+        "roofline": {"bound": "hbm", "kernel": "attn_kernel (sparse attention over kept pages)",
+                     "achieved": att_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": att_gbs / peak, "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": att_b, "ms_per_launch": att_ms,
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "step_hbm": {"achieved_gbs": step_gbs, "frac": step_gbs / peak,
+                     "algorithmic_bytes": sel_b + att_b},
+        "kernels_ms": {"select_pages": sel_ms, "sparse_attention": att_ms,
+                       "select_gbs": sel_b / (sel_ms * 1e-3) / 1e9},
+        "dense": {"ms_per_step": dense_ms, "queries_per_s": B / (dense_ms * 1e-3),
+                  "achieved_gbs": dense_b / (dense_ms * 1e-3) / 1e9,
+                  "frac": dense_b / (dense_ms * 1e-3) / 1e9 / peak,
+                  "speedup_sparse_over_dense": dense_ms / ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * B / (e2e_mean * 1e-3), "unit": "queries/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="headline_8k")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline (0 to skip)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,201 @@
+/*
+ * qasa.h -- C ABI of the query-aware sparse paged decode library (GB300, sm_103a).
+ *
+ * Method: "TinyServe: Query-Aware Cache Selection for Efficient LLM Serving"
+ * (arXiv 2509.12211).  Section 方法详解 / 关键设计 of that summary: every KV-cache
+ * block (page) carries a bounding box of what it holds; at decode time the
+ * query is compared with every page's box and only the most similar pages are
+ * loaded; the abstract: page scoring, sparse memory access and masked
+ * attention form one decode step.  The edgentiq post ("How TinyServe Works")
+ * names the retriever (page selection over page-level metadata) and the sparse
+ * attention executor (attention over the selected pages only).
+ *
+ * Readings fixed by this library (the pages give no formula or layout):
+ *   box      lo[c] / hi[c] = per-channel min / max of the keys in the page's
+ *            valid slots, stored in the KV dtype (min/max are exact).
+ *   score    s(p) = max over the G query heads of the group of
+ *            sum_c max(q_c * lo_c, q_c * hi_c), accumulated in fp32.
+ *   select   logical page 0 (sink) and page N-1 (newest) always kept; the rest
+ *            of a budget of k pages goes to the highest scores, equal scores
+ *            to the lower page index; k >= N keeps every page.  Kept ids are
+ *            written in ascending order.
+ *   attend   softmax(scale * q.k) over the tokens of the kept pages whose
+ *            position is < seq_len, times V; scale <= 0 selects 1/sqrt(d);
+ *            fp32 accumulation; the output has the KV dtype.
+ *
+ * Layout (all row-major, caller-owned DEVICE memory unless stated):
+ *   k_pool, v_pool  [num_phys_pages][num_kv_heads][page_size][head_dim]
+ *   page_bounds     [num_phys_pages][num_kv_heads][2][head_dim]  (lo row, hi row)
+ *   block_table     [batch][max_pages_per_seq] int32: physical page of each
+ *                   logical page of each sequence
+ *   q, out          [batch][num_q_heads][head_dim]; query head j uses KV head
+ *                   j / (num_q_heads / num_kv_heads)
+ *   selected        [batch][num_kv_heads][max_budget] int32, -1 padded
+ *
+ * Supported: dtype f32 / f16 / bf16; head_dim 64 or 128; page_size 16 or 32;
+ * group size G = num_q_heads / num_kv_heads in 1..8; max_pages_per_seq up to
+ * 16384; every device pointer 16-byte aligned.
+ *
+ * Ownership and threading: the library allocates nothing, keeps no state
+ * between calls and only enqueues work on the given stream (asynchronous).
+ * Calls on different streams that share a workspace race.
+ *
+ * Errors: argument problems found on the host return a nonzero status before
+ * any launch.  Problems in device data (a block-table entry outside
+ * [0, num_phys_pages), a seq_len beyond the block table, a budget above
+ * max_budget, a bounded wait that gave up) never trap: the kernel skips the
+ * offending page (or clamps the length/budget), ORs a QASA_DEVERR_* bit into
+ * *device_status when that pointer is non-NULL, and finishes.
+ */
+#ifndef QASA_H
+#define QASA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QASA_DTYPE_F32 = 0,
+    QASA_DTYPE_F16 = 1,
+    QASA_DTYPE_BF16 = 2
+} qasa_dtype;
+
+typedef enum {
+    QASA_OK = 0,
+    QASA_ERR_NULL = 1,         /* a required pointer is NULL */
+    QASA_ERR_DTYPE = 2,        /* unknown dtype */
+    QASA_ERR_SHAPE = 3,        /* unsupported head_dim / page_size / group / sizes */
+    QASA_ERR_ALIGN = 4,        /* a device pointer is not 16-byte aligned */
+    QASA_ERR_BUDGET = 5,       /* max_budget < 2 */
+    QASA_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than qasa_decode_workspace_size */
+    QASA_ERR_CUDA = 7,         /* a CUDA runtime call or launch failed */
+    QASA_ERR_DRIVER = 8        /* the tensor-map encoder could not be obtained or failed */
+} qasa_status;
+
+/* Bits ORed into *device_status by the kernels. */
+#define QASA_DEVERR_PAGE_ID   0x1  /* block-table entry outside [0, num_phys_pages): page skipped */
+#define QASA_DEVERR_SEQ_LEN   0x2  /* seq_len < 0 or beyond max_pages_per_seq*page_size: clamped */
+#define QASA_DEVERR_BUDGET    0x4  /* kept pages would exceed max_budget: clamped */
+#define QASA_DEVERR_TIMEOUT   0x8  /* a bounded wait in a pipelined kernel gave up */
+#define QASA_DEVERR_APPEND    0x10 /* append_lens[b] outside [0, max_new_tokens]: clamped */
+#define QASA_DEVERR_SELECTED  0x20 /* a selected id outside [0, N_b): page skipped */
+
+typedef struct {
+    void *k_pool;            /* [num_phys_pages][num_kv_heads][page_size][head_dim] */
+    void *v_pool;            /* same shape as k_pool */
+    void *page_bounds;       /* [num_phys_pages][num_kv_heads][2][head_dim] */
+    int32_t num_phys_pages;
+    int32_t num_kv_heads;
+    int32_t page_size;
+    int32_t head_dim;
+    qasa_dtype dtype;
+} qasa_kv_cache;
+
+/*
+ * Append new tokens to every sequence and keep the page boxes current
+ * (the bounding-box metadata of 方法详解 / 关键设计; maintained at write time).
+ *
+ * Sequence b has seq_lens[b] tokens before the call; its new tokens are
+ * k_new[b][t] / v_new[b][t] for t < n_b, where n_b = append_lens[b] if
+ * append_lens is non-NULL, else max_new_tokens.  Token at position
+ * pos = seq_lens[b] + t goes to slot pos % page_size of physical page
+ * block_table[b][pos / page_size], in both pools.  The page's box becomes the
+ * min / max of its previous box and the new keys, except that a page whose
+ * slot 0 is written by this call starts a fresh box.
+ *   k_new, v_new   [batch][max_new_tokens][num_kv_heads][head_dim], cache dtype
+ *   seq_lens       [batch] int32, lengths BEFORE the call (not modified: the
+ *                  caller advances them)
+ *   append_lens    [batch] int32 or NULL
+ *   device_status  int32 or NULL (see QASA_DEVERR_*)
+ * A page written by one call must belong to one sequence only.
+ */
+qasa_status qasa_kv_append(const qasa_kv_cache *cache, const int32_t *block_table,
+                           int32_t max_pages_per_seq, const int32_t *seq_lens,
+                           const int32_t *append_lens, const void *k_new, const void *v_new,
+                           int32_t batch, int32_t max_new_tokens, int32_t *device_status,
+                           cudaStream_t stream);
+
+/*
+ * Bytes of device workspace the decode calls need for this shape on the
+ * CURRENT device (split-K partials and per-(sequence, KV head) counters).
+ * The workspace is scratch: its contents need no initialisation and are
+ * meaningless between calls.
+ */
+size_t qasa_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                  const qasa_kv_cache *cache, int32_t max_pages_per_seq);
+
+/*
+ * Query-aware page selection alone: score every page of every
+ * (sequence, KV head) against the box metadata and keep the budget
+ * (方法详解 / 关键设计: similarity of the query to each block's box, the most
+ * similar blocks are loaded).
+ *   q              [batch][num_q_heads][head_dim], cache dtype
+ *   budget_pages   [batch] int32: requested pages per sequence.  The kept count
+ *                  is k_b = min(N_b, max(budget_pages[b], forced)) with
+ *                  forced = min(N_b, 2); k_b > max_budget is clamped and flagged.
+ *   selected       [batch][num_kv_heads][max_budget] int32 out: ascending
+ *                  logical page ids, -1 padded
+ *   scores_out     [batch][num_kv_heads][max_pages_per_seq] float out, or NULL;
+ *                  entries >= N_b are left untouched
+ */
+qasa_status qasa_select_pages(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
+                              const int32_t *block_table, int32_t max_pages_per_seq,
+                              const int32_t *seq_lens, const int32_t *budget_pages,
+                              int32_t max_budget, int32_t *selected, float *scores_out,
+                              void *workspace, size_t workspace_bytes, int32_t batch,
+                              int32_t *device_status, cudaStream_t stream);
+
+/*
+ * Masked attention over a given selection (the sparse attention executor of
+ * the edgentiq post): for every (sequence, KV head) the first k_b entries of
+ * its `selected` row (k_b as in qasa_select_pages) are logical page ids.
+ *   out            [batch][num_q_heads][head_dim], cache dtype
+ * A sequence with seq_len 0 gets zeros.
+ */
+qasa_status qasa_sparse_attention(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
+                                  const int32_t *block_table, int32_t max_pages_per_seq,
+                                  const int32_t *seq_lens, const int32_t *budget_pages,
+                                  int32_t max_budget, const int32_t *selected, float scale,
+                                  void *out, void *workspace, size_t workspace_bytes,
+                                  int32_t batch, int32_t *device_status, cudaStream_t stream);
+
+/*
+ * One decode step: qasa_select_pages followed by qasa_sparse_attention on the
+ * same stream (the second kernel's prologue overlaps the first's tail through
+ * programmatic dependent launch).  Arguments as in those two calls.
+ */
+qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void *q,
+                                         int32_t num_q_heads, const int32_t *block_table,
+                                         int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                         const int32_t *budget_pages, int32_t max_budget,
+                                         float scale, void *out, int32_t *selected,
+                                         float *scores_out, void *workspace,
+                                         size_t workspace_bytes, int32_t batch,
+                                         int32_t *device_status, cudaStream_t stream);
+
+/*
+ * Dense paged decode attention over every page (the comparison path: what the
+ * decode step costs without selection).  Arguments as in qasa_sparse_attention.
+ */
+qasa_status qasa_dense_decode_attention(const qasa_kv_cache *cache, const void *q,
+                                        int32_t num_q_heads, const int32_t *block_table,
+                                        int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                        float scale, void *out, void *workspace,
+                                        size_t workspace_bytes, int32_t batch,
+                                        int32_t *device_status, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char *qasa_status_string(qasa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t qasa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QASA_H */

@@ -1,0 +1,353 @@
+// api.cu -- C entry points of libqasa: argument checks, workspace carve-up,
+// TMA descriptor encoding and kernel launches.  Every declaration lives in
+// include/qasa.h together with its contract.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "qasa_launch.h"
+
+using namespace qasa;
+
+namespace {
+
+constexpr int kMaxPagesPerSeq = 16384;
+constexpr int kMaxBatch = 8192;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_size(qasa_dtype dt) { return dt == QASA_DTYPE_F32 ? 4 : 2; }
+
+qasa_status check_cache(const qasa_kv_cache *c) {
+    if (!c || !c->k_pool || !c->v_pool || !c->page_bounds) return QASA_ERR_NULL;
+    if (c->dtype != QASA_DTYPE_F32 && c->dtype != QASA_DTYPE_F16 && c->dtype != QASA_DTYPE_BF16)
+        return QASA_ERR_DTYPE;
+    if (c->head_dim != 64 && c->head_dim != 128) return QASA_ERR_SHAPE;
+    if (c->page_size != 16 && c->page_size != 32) return QASA_ERR_SHAPE;
+    if (c->num_kv_heads < 1 || c->num_phys_pages < 1) return QASA_ERR_SHAPE;
+    if ((long long)c->num_phys_pages * c->num_kv_heads * c->page_size > 0x7fffffffLL)
+        return QASA_ERR_SHAPE;
+    if (!aligned16(c->k_pool) || !aligned16(c->v_pool) || !aligned16(c->page_bounds))
+        return QASA_ERR_ALIGN;
+    return QASA_OK;
+}
+
+qasa_status check_decode(const qasa_kv_cache *c, const void *q, int num_q_heads,
+                         const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                         const void *out, int batch) {
+    qasa_status st = check_cache(c);
+    if (st != QASA_OK) return st;
+    if (!q || !block_table || !seq_lens || !out) return QASA_ERR_NULL;
+    if (batch < 0 || batch > kMaxBatch) return QASA_ERR_SHAPE;
+    if (num_q_heads < 1 || num_q_heads % c->num_kv_heads != 0) return QASA_ERR_SHAPE;
+    const int G = num_q_heads / c->num_kv_heads;
+    if (G > 8) return QASA_ERR_SHAPE;
+    if (max_pages < 1 || max_pages > kMaxPagesPerSeq) return QASA_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(out)) return QASA_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return QASA_ERR_ALIGN;
+    return QASA_OK;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+size_t smem_optin() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    return (size_t)n;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace carve-up: counters [units] | partial (m, l) [(units + C) * G * 2] |
+// partial o [(units + C) * G * D], each region 256-byte aligned.
+struct WsLayout {
+    size_t counters, part_ml, part_o, total;
+};
+
+WsLayout ws_layout(int batch, int num_q_heads, const qasa_kv_cache *c, int grid) {
+    const size_t units = (size_t)batch * c->num_kv_heads;
+    const size_t G = (size_t)(num_q_heads / c->num_kv_heads);
+    const size_t slots = units + (size_t)grid;
+    WsLayout w;
+    w.counters = 0;
+    w.part_ml = align_up(units * 4, 256);
+    w.part_o = w.part_ml + align_up(slots * G * 2 * 4, 256);
+    w.total = w.part_o + align_up(slots * G * (size_t)c->head_dim * 4, 256);
+    return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D view of a KV pool: rows = (page, head, slot), columns = head_dim; one
+// TMA box = 128 bytes of columns x page_size rows, 128-byte swizzle.
+qasa_status pool_tensor_map(CUtensorMap *map, void *base, const qasa_kv_cache *c) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return QASA_ERR_DRIVER;
+    const size_t es = elem_size(c->dtype);
+    const CUtensorMapDataType t = c->dtype == QASA_DTYPE_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : c->dtype == QASA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[2] = {(cuuint64_t)c->head_dim,
+                          (cuuint64_t)c->num_phys_pages * c->num_kv_heads * c->page_size};
+    cuuint64_t strides[1] = {(cuuint64_t)c->head_dim * es};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)c->page_size};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, t, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QASA_OK : QASA_ERR_DRIVER;
+}
+
+qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_heads,
+                       const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                       const int32_t *budget_pages, int max_budget, int32_t *selected,
+                       float *scores_out, int32_t *counters, int batch, int32_t *status,
+                       cudaStream_t stream) {
+    SelectParams p;
+    p.bounds = cache->page_bounds;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.budget = budget_pages;
+    p.q = q;
+    p.selected = selected;
+    p.scores_out = scores_out;
+    p.counters = counters;
+    p.status = status;
+    p.num_phys = cache->num_phys_pages;
+    p.Hkv = cache->num_kv_heads;
+    p.P = cache->page_size;
+    p.G = num_q_heads / cache->num_kv_heads;
+    p.Hq = num_q_heads;
+    p.max_pages = max_pages;
+    p.max_budget = max_budget;
+    cudaError_t e = launch_select(cache->dtype, cache->head_dim, p, batch * cache->num_kv_heads, stream);
+    return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
+}
+
+qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_heads,
+                          const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                          const int32_t *budget_pages, int max_budget, const int32_t *selected,
+                          float scale, void *out, void *workspace, size_t ws_bytes, int batch,
+                          int32_t *status, bool dense, bool pdl, cudaStream_t stream) {
+    const int grid = sm_count();
+    if (grid <= 0) return QASA_ERR_CUDA;
+    const WsLayout w = ws_layout(batch, num_q_heads, cache, grid);
+    if (!workspace) return QASA_ERR_WORKSPACE;
+    if (ws_bytes < w.total || !aligned16(workspace)) return QASA_ERR_WORKSPACE;
+    CUtensorMap km, vm;
+    qasa_status st = pool_tensor_map(&km, cache->k_pool, cache);
+    if (st != QASA_OK) return st;
+    st = pool_tensor_map(&vm, cache->v_pool, cache);
+    if (st != QASA_OK) return st;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    if (dense && cudaMemsetAsync(ws + w.counters, 0, (size_t)batch * cache->num_kv_heads * 4, stream) != cudaSuccess)
+        return QASA_ERR_CUDA;
+    AttnParams p;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.budget = budget_pages;
+    p.selected = selected;
+    p.q = q;
+    p.out = out;
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    p.part_ml = reinterpret_cast<float *>(ws + w.part_ml);
+    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+    p.status = status;
+    p.B = batch;
+    p.Hkv = cache->num_kv_heads;
+    p.G = num_q_heads / cache->num_kv_heads;
+    p.Hq = num_q_heads;
+    p.max_pages = max_pages;
+    p.max_budget = max_budget;
+    p.num_phys = cache->num_phys_pages;
+    const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)cache->head_dim);
+    p.scale_log2 = (float)(sc * 1.4426950408889634);
+    p.dense = dense ? 1 : 0;
+    p.stages = 0;
+    p.wait_limit_ns = kWaitLimitNs;
+    size_t budget = smem_optin();
+    if (budget == 0) return QASA_ERR_CUDA;
+    budget = budget > 1024 ? budget - 1024 : budget;   // leave room for static shared memory
+    cudaError_t e = launch_attention(cache->dtype, cache->head_dim, cache->page_size, km, vm, p, grid,
+                                     budget, pdl, stream);
+    if (e == cudaErrorInvalidConfiguration) return QASA_ERR_SHAPE;
+    return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+qasa_status qasa_kv_append(const qasa_kv_cache *cache, const int32_t *block_table,
+                           int32_t max_pages_per_seq, const int32_t *seq_lens,
+                           const int32_t *append_lens, const void *k_new, const void *v_new,
+                           int32_t batch, int32_t max_new_tokens, int32_t *device_status,
+                           cudaStream_t stream) {
+    qasa_status st = check_cache(cache);
+    if (st != QASA_OK) return st;
+    if (batch == 0 || max_new_tokens == 0) return QASA_OK;
+    if (!block_table || !seq_lens || !k_new || !v_new) return QASA_ERR_NULL;
+    if (batch < 0 || max_new_tokens < 0 || max_pages_per_seq < 1 || max_pages_per_seq > kMaxPagesPerSeq)
+        return QASA_ERR_SHAPE;
+    if (batch > 65535) return QASA_ERR_SHAPE;
+    if (!aligned16(k_new) || !aligned16(v_new)) return QASA_ERR_ALIGN;
+    if (batch == 0 || max_new_tokens == 0) return QASA_OK;
+    AppendParams p;
+    p.k_pool = cache->k_pool;
+    p.v_pool = cache->v_pool;
+    p.bounds = cache->page_bounds;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.append_lens = append_lens;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.status = device_status;
+    p.num_phys = cache->num_phys_pages;
+    p.Hkv = cache->num_kv_heads;
+    p.P = cache->page_size;
+    p.max_pages = max_pages_per_seq;
+    p.T = max_new_tokens;
+    cudaError_t e = launch_append(cache->dtype, cache->head_dim, p, batch, stream);
+    return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
+}
+
+size_t qasa_decode_workspace_size(int32_t batch, int32_t num_q_heads, const qasa_kv_cache *cache,
+                                  int32_t max_pages_per_seq) {
+    (void)max_pages_per_seq;
+    if (!cache || cache->num_kv_heads < 1 || batch < 0 || num_q_heads < cache->num_kv_heads) return 0;
+    const int grid = sm_count();
+    if (grid <= 0) return 0;
+    return ws_layout(batch, num_q_heads, cache, grid).total;
+}
+
+qasa_status qasa_select_pages(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
+                              const int32_t *block_table, int32_t max_pages_per_seq,
+                              const int32_t *seq_lens, const int32_t *budget_pages,
+                              int32_t max_budget, int32_t *selected, float *scores_out,
+                              void *workspace, size_t workspace_bytes, int32_t batch,
+                              int32_t *device_status, cudaStream_t stream) {
+    if (batch == 0) return check_cache(cache);
+    qasa_status st = check_decode(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                                  selected, batch);
+    if (st != QASA_OK) return st;
+    if (!budget_pages) return QASA_ERR_NULL;
+    if (max_budget < 2) return QASA_ERR_BUDGET;
+    if (!workspace) return QASA_ERR_WORKSPACE;
+    const int grid = sm_count();
+    if (grid <= 0) return QASA_ERR_CUDA;
+    if (workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total) return QASA_ERR_WORKSPACE;
+    if (batch == 0) return QASA_OK;
+    return run_select(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
+                      max_budget, selected, scores_out, static_cast<int32_t *>(workspace), batch,
+                      device_status, stream);
+}
+
+qasa_status qasa_sparse_attention(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
+                                  const int32_t *block_table, int32_t max_pages_per_seq,
+                                  const int32_t *seq_lens, const int32_t *budget_pages,
+                                  int32_t max_budget, const int32_t *selected, float scale,
+                                  void *out, void *workspace, size_t workspace_bytes,
+                                  int32_t batch, int32_t *device_status, cudaStream_t stream) {
+    if (batch == 0) return check_cache(cache);
+    qasa_status st = check_decode(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                                  out, batch);
+    if (st != QASA_OK) return st;
+    if (!budget_pages || !selected) return QASA_ERR_NULL;
+    if (max_budget < 2) return QASA_ERR_BUDGET;
+    if (batch == 0) return QASA_OK;
+    // counters must start at zero: the selection kernel normally clears them
+    const int grid = sm_count();
+    if (grid <= 0) return QASA_ERR_CUDA;
+    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total)
+        return QASA_ERR_WORKSPACE;
+    if (cudaMemsetAsync(workspace, 0, (size_t)batch * cache->num_kv_heads * 4, stream) != cudaSuccess)
+        return QASA_ERR_CUDA;
+    return run_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
+                         max_budget, selected, scale, out, workspace, workspace_bytes, batch,
+                         device_status, false, false, stream);
+}
+
+qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void *q,
+                                         int32_t num_q_heads, const int32_t *block_table,
+                                         int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                         const int32_t *budget_pages, int32_t max_budget,
+                                         float scale, void *out, int32_t *selected,
+                                         float *scores_out, void *workspace,
+                                         size_t workspace_bytes, int32_t batch,
+                                         int32_t *device_status, cudaStream_t stream) {
+    if (batch == 0) return check_cache(cache);
+    qasa_status st = check_decode(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                                  out, batch);
+    if (st != QASA_OK) return st;
+    if (!budget_pages || !selected) return QASA_ERR_NULL;
+    if (max_budget < 2) return QASA_ERR_BUDGET;
+    const int grid = sm_count();
+    if (grid <= 0) return QASA_ERR_CUDA;
+    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total ||
+        !aligned16(workspace))
+        return QASA_ERR_WORKSPACE;
+    if (batch == 0) return QASA_OK;
+    st = run_select(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
+                    max_budget, selected, scores_out, static_cast<int32_t *>(workspace), batch,
+                    device_status, stream);
+    if (st != QASA_OK) return st;
+    return run_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
+                         max_budget, selected, scale, out, workspace, workspace_bytes, batch,
+                         device_status, false, true, stream);
+}
+
+qasa_status qasa_dense_decode_attention(const qasa_kv_cache *cache, const void *q,
+                                        int32_t num_q_heads, const int32_t *block_table,
+                                        int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                        float scale, void *out, void *workspace,
+                                        size_t workspace_bytes, int32_t batch,
+                                        int32_t *device_status, cudaStream_t stream) {
+    if (batch == 0) return check_cache(cache);
+    qasa_status st = check_decode(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                                  out, batch);
+    if (st != QASA_OK) return st;
+    if (batch == 0) return QASA_OK;
+    return run_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, seq_lens,
+                         2, nullptr, scale, out, workspace, workspace_bytes, batch, device_status,
+                         true, false, stream);
+}
+
+const char *qasa_status_string(qasa_status s) {
+    switch (s) {
+    case QASA_OK: return "ok";
+    case QASA_ERR_NULL: return "a required pointer is NULL";
+    case QASA_ERR_DTYPE: return "unknown dtype";
+    case QASA_ERR_SHAPE: return "unsupported shape (head_dim, page_size, group size or sizes)";
+    case QASA_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+    case QASA_ERR_BUDGET: return "max_budget must be at least 2";
+    case QASA_ERR_WORKSPACE: return "workspace missing or too small";
+    case QASA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case QASA_ERR_DRIVER: return "the TMA descriptor encoder is unavailable or rejected the pool";
+    }
+    return "unknown status";
+}
+
+int32_t qasa_version(void) { return 100; }
+
+}  // extern "C"

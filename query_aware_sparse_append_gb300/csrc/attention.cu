@@ -1,0 +1,598 @@
+// attention.cu -- masked paged decode attention over the selected pages.
+//
+// The sparse-attention half of TinyServe's decode step ("TinyServe:
+// Query-Aware Cache Selection for Efficient LLM Serving", abstract: sparse
+// memory access and masked attention; edgentiq post, "How TinyServe Works":
+// the sparse attention executor computes attention over the selected KV pages
+// only).  For every (sequence b, KV head h) and each of its G query heads:
+//
+//     out = sum_t softmax_t(scale * q.k_t) v_t   over the tokens t of the kept
+//                                               pages whose position < seq_len
+//
+// Work split (persistent, balanced).  All kept (unit, page) pairs of the batch
+// are laid out in one flattened order (unit-major, pages ascending); CTA c of C
+// takes the contiguous range [c*T/C, (c+1)*T/C).  A range covers whole units
+// (written straight to `out`) and at most two partial units at its ends,
+// whose partial (m, l, o) go to workspace slot (unit + c); the CTA that
+// finishes a unit last (atomic ticket, no waiting) merges its partials.
+//
+// Inside a CTA: warp 0 is the producer.  It turns kept page ids into physical
+// tiles through the block table and issues one tiled TMA box per 128 bytes of
+// head dimension for K and for V (cp.async.bulk.tensor, 128-byte swizzle) into
+// a ring of shared-memory stages guarded by mbarriers.  The other NW warps
+// consume pages round-robin.  For 16-bit KV and G >= 2 a consumer computes
+// S^T = K q^T and O^T += V^T P^T as m16n8k16 tensor-core MMAs (16 tokens x 8
+// query heads per MMA; ldmatrix reads the swizzled tiles conflict-free;
+// movmatrix turns the S accumulators into the P operand) with an online
+// softmax in fp32.  Otherwise (fp32 KV, or one query head per KV head, where
+// q.K is not a real contraction) it uses FFMA and warp shuffles.
+//
+// Every wait is bounded: a wait that gives up sets QASA_DEVERR_TIMEOUT, the CTA
+// stops issuing, drains the copies it issued (again bounded) and returns.
+#include "qasa_device.cuh"
+#include "qasa_launch.h"
+
+namespace qasa {
+
+
+struct StageInfo {
+    int page;    // logical page id
+    int nvalid;  // valid tokens in the page (0: nothing to attend)
+};
+
+// Host-side size of the dynamic shared memory (mirrors the device carve-up).
+size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int P, bool mma, int B) {
+    size_t s = 1024;                                   // alignment slack for the ring
+    s += (size_t)stages * stage_bytes;
+    s += (size_t)stages * 2 * sizeof(uint64_t);        // full / empty barriers
+    s += (size_t)stages * sizeof(StageInfo);
+    s += (size_t)nw * gmax * (D + 2) * sizeof(float);  // combine scratch
+    if (!mma) s += (size_t)nw * gmax * (D + P) * sizeof(float);
+    s += (size_t)(2 * B + 2) * sizeof(int);            // prefix, lengths
+    s += 64;
+    return s;
+}
+
+__device__ __forceinline__ long long range_start(int c, int C, long long T) {
+    return (long long)c * T / C;
+}
+// CTA whose range holds flattened index g (0 <= g < T).
+__device__ __forceinline__ int cta_of(long long g, int C, long long T) {
+    return (int)(((g + 1) * C - 1) / T);
+}
+
+template <typename T, int D, int P, bool MMA, int GMAX, int NW>
+__global__ void __launch_bounds__(32 * (NW + 1), 1)
+attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+            AttnParams p) {
+    constexpr int ES = (int)sizeof(T);
+    constexpr int TILE = P * D * ES;            // one (page, head) tile of K or V
+    constexpr int STAGE = 2 * TILE;
+    constexpr int NSUB = D * ES / 128;          // 128-byte column boxes per tile
+    constexpr int BOXW = 128 / ES;              // elements per box row
+    constexpr int NCT = NW * 32;                // consumer threads
+    static_assert(TILE % 1024 == 0, "tile must keep 1024-byte swizzle alignment");
+
+    extern __shared__ unsigned char smem_raw[];
+    const int S = p.stages;
+    unsigned char *ring = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)S * STAGE);
+    uint64_t *empty_bar = full_bar + S;
+    StageInfo *info = reinterpret_cast<StageInfo *>(empty_bar + S);
+    float *scr_o = reinterpret_cast<float *>(info + S);           // [NW][GMAX][D]
+    float *scr_m = scr_o + NW * GMAX * D;                          // [NW][GMAX]
+    float *scr_l = scr_m + NW * GMAX;                              // [NW][GMAX]
+    float *ff_q = scr_l + NW * GMAX;                               // FFMA only: [NW][GMAX][D]
+    float *ff_p = ff_q + (MMA ? 0 : NW * GMAX * D);                // FFMA only: [NW][GMAX][P]
+    int *prefix = reinterpret_cast<int *>(ff_p + (MMA ? 0 : NW * GMAX * P));   // [B + 1]
+    int *lens = prefix + (p.B + 1);                                // [B]
+    __shared__ int s_flag;       // last-arriver flag
+    __shared__ int s_abort;      // a bounded wait gave up
+    volatile int *abort_flag = &s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = gridDim.x, c = blockIdx.x;
+    const int Hkv = p.Hkv, G = p.G;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (tid == 32) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    // per-sequence kept counts (same rule as the selection kernel) and their prefix
+    {
+        int carry = 0;
+        __shared__ int s_wsum[32];
+        for (int base = 0; base < p.B; base += blockDim.x) {
+            const int b = base + tid;
+            int cnt = 0;
+            if (b < p.B) {
+                const int L = valid_len(p.seq_lens[b], p.max_pages, P, c == 0 ? p.status : nullptr);
+                const int N = (L + P - 1) / P;
+                cnt = p.dense ? N : kept_pages(N, p.budget[b], p.max_budget, nullptr, false);
+                lens[b] = L;
+            }
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                int t = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += t;
+            }
+            if (lane == 31) s_wsum[warp] = incl;
+            __syncthreads();
+            int wbase = 0;
+            for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
+            int total = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += s_wsum[w];
+            if (b < p.B) prefix[b] = carry + wbase + incl - cnt;
+            carry += total;
+            __syncthreads();
+        }
+        if (tid == 0) prefix[p.B] = carry;
+    }
+    __syncthreads();
+    const long long Ttot = (long long)Hkv * prefix[p.B];
+    const long long g0 = range_start(c, C, Ttot), g1 = range_start(c + 1, C, Ttot);
+
+    // sequences with no pages: zero their outputs (unit u handled by CTA u % C)
+    for (int b = 0; b < p.B; ++b) {
+        if (prefix[b + 1] != prefix[b]) continue;
+        for (int h = 0; h < Hkv; ++h) {
+            if ((b * Hkv + h) % C != c) continue;
+            T *o = static_cast<T *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+            for (int i = tid; i < G * D; i += blockDim.x) o[i] = elem<T>::from_f(0.f);
+        }
+    }
+
+    pdl_wait();   // selected ids and counters come from the preceding kernel
+
+    // locate flattened index g: sequence b, KV head h, position j in the unit
+    auto locate = [&](long long g, int &b, int &h, int &j, long long &ustart, int &cnt) {
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {   // largest b with Hkv * prefix[b] <= g
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)Hkv * prefix[mid] <= g) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        cnt = prefix[b + 1] - prefix[b];
+        const long long off = g - (long long)Hkv * prefix[b];
+        h = (int)(off / cnt);
+        j = (int)(off - (long long)h * cnt);
+        ustart = (long long)Hkv * prefix[b] + (long long)h * cnt;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        long long issued_hi = g0;   // pages [g0, issued_hi) had their copies issued
+        for (long long base = g0; base < g1 && !*abort_flag; base += 32) {
+            const long long g = base + lane;
+            int nvalid = 0, row = 0, page = -1;
+            if (g < g1) {
+                int b, h, j, cnt;
+                long long us;
+                locate(g, b, h, j, us, cnt);
+                const int L = lens[b];
+                const int N = (L + P - 1) / P;
+                page = p.dense ? j : p.selected[((size_t)b * Hkv + h) * p.max_budget + j];
+                if (page < 0 || page >= N) {
+                    if (p.status) atomicOr(p.status, QASA_DEVERR_SELECTED);
+                } else {
+                    const int phys = p.block_table[(size_t)b * p.max_pages + page];
+                    if (phys < 0 || phys >= p.num_phys) {
+                        if (p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
+                    } else {
+                        nvalid = min(P, L - page * P);
+                        row = (int)(((long long)phys * Hkv + h) * P);
+                    }
+                }
+            }
+            const int n = (int)min((long long)32, g1 - base);
+            for (int i = 0; i < n; ++i) {
+                const int nv = __shfl_sync(0xffffffffu, nvalid, i);
+                const int rw = __shfl_sync(0xffffffffu, row, i);
+                const int pg = __shfl_sync(0xffffffffu, page, i);
+                if (lane == 0 && !*abort_flag) {
+                    const long long idx = base + i - g0;
+                    const int s = (int)(idx % S);
+                    const uint32_t ph = (uint32_t)((idx / S) & 1);
+                    if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, p.wait_limit_ns)) {
+                        if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                    } else {
+                        info[s].page = pg;
+                        info[s].nvalid = nv;
+                        unsigned char *st = ring + (size_t)s * STAGE;
+                        if (nv > 0) {
+                            mbar_arrive_expect_tx(&full_bar[s], STAGE);
+#pragma unroll
+                            for (int x = 0; x < NSUB; ++x) {
+                                tma_load_2d(st + x * P * 128, &kmap, &full_bar[s], x * BOXW, rw);
+                                tma_load_2d(st + TILE + x * P * 128, &vmap, &full_bar[s], x * BOXW, rw);
+                            }
+                        } else {
+                            mbar_arrive(&full_bar[s]);
+                        }
+                        issued_hi = base + i + 1;
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        // drain: wait until every copy this CTA issued has landed (bounded)
+        if (lane == 0) {
+            const long long nissued = issued_hi - g0;
+            for (long long idx = (nissued > S ? nissued - S : 0); idx < nissued; ++idx) {
+                const int s = (int)(idx % S);
+                const uint32_t ph = (uint32_t)((idx / S) & 1);
+                if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
+                    if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int w = warp - 1;
+    const int ct = tid - 32;
+    long long g = g0;
+    while (g < g1) {
+        int b, h, j0, cnt;
+        long long us;
+        locate(g, b, h, j0, us, cnt);
+        const long long ue = us + cnt;
+        const long long s1 = min(g1, ue);
+        const int u = b * Hkv + h;
+        const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+
+        // first flattened offset in [g - g0, s1 - g0) that belongs to this warp
+        const long long first = g - g0, lastx = s1 - g0;
+        long long i = first + ((w - first % NW) % NW + NW) % NW;
+
+        if constexpr (MMA) {
+            const int cq = lane & 3, nq = lane >> 2;
+            uint32_t qf[D / 16][2];
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                qf[ks][0] = 0u; qf[ks][1] = 0u;
+                if (nq < G) {
+                    const T *qr = qb + (size_t)nq * D + ks * 16 + 2 * cq;
+                    qf[ks][0] = *reinterpret_cast<const uint32_t *>(qr);
+                    qf[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+                }
+            }
+            float o[D / 16][4];
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+            float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+            for (; i < lastx; i += NW) {
+                const int s = (int)(i % S);
+                const uint32_t ph = (uint32_t)((i / S) & 1);
+                if (*abort_flag) break;
+                if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
+                    if (lane == 0 && p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                const int nvalid = info[s].nvalid;
+                unsigned char *kst = ring + (size_t)s * STAGE;
+                unsigned char *vst = kst + TILE;
+                const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
+                if (nvalid > 0 && nvalid < P) {
+                    // rows past the sequence end may hold anything: zero V there so that
+                    // the masked (zero) weights cannot meet a NaN in the P.V product
+                    const int rows = ((nvalid + 15) & ~15) - nvalid;
+                    for (int e = lane; e < rows * NSUB * 8; e += 32) {
+                        const int r = nvalid + e / (NSUB * 8), ch = e % (NSUB * 8);
+                        *reinterpret_cast<uint4 *>(vst + swz128_offset<P>(r, ch)) = make_uint4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int sub = 0; sub < P / 16; ++sub) {
+                    if (sub * 16 >= nvalid) break;
+                    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const int tok = sub * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                        const int chn = 2 * ks + (lane >> 4);
+                        uint32_t a[4];
+                        ldmatrix_x4(kbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
+                        if (ks & 1) mma16816<T>::run(sb, a, qf[ks][0], qf[ks][1]);
+                        else mma16816<T>::run(sa, a, qf[ks][0], qf[ks][1]);
+                    }
+                    const int t0 = sub * 16 + (lane >> 2), t1 = t0 + 8;
+                    const bool v0 = t0 < nvalid, v1 = t1 < nvalid;
+                    const float z0 = v0 ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
+                    const float z1 = v0 ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
+                    const float z2 = v1 ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
+                    const float z3 = v1 ? (sa[3] + sb[3]) * p.scale_log2 : -INFINITY;
+                    float x0 = fmaxf(z0, z2), x1 = fmaxf(z1, z3);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+                        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+                    }
+                    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+                    const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+                    const float p0 = exp2f(z0 - n0), p1 = exp2f(z1 - n1);
+                    const float p2 = exp2f(z2 - n0), p3 = exp2f(z3 - n1);
+                    l0 = l0 * al0 + p0 + p2;
+                    l1 = l1 * al1 + p1 + p3;
+                    m0 = n0; m1 = n1;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+                    }
+                    const uint32_t pb0 = movmatrix_trans(mma16816<T>::pack2(p0, p1));
+                    const uint32_t pb1 = movmatrix_trans(mma16816<T>::pack2(p2, p3));
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const int tok = sub * 16 + (lane & 7) + (lane >> 4) * 8;
+                        const int chn = 2 * mt + ((lane >> 3) & 1);
+                        uint32_t a[4];
+                        ldmatrix_x4_trans(vbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
+                        mma16816<T>::run(o[mt], a, pb0, pb1);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[s]);
+            }
+            // export this warp's state
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
+            const int h0 = 2 * cq, h1 = 2 * cq + 1;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int ch = mt * 16 + nq;
+                if (h0 < G) {
+                    scr_o[(w * GMAX + h0) * D + ch] = o[mt][0];
+                    scr_o[(w * GMAX + h0) * D + ch + 8] = o[mt][2];
+                }
+                if (h1 < G) {
+                    scr_o[(w * GMAX + h1) * D + ch] = o[mt][1];
+                    scr_o[(w * GMAX + h1) * D + ch + 8] = o[mt][3];
+                }
+            }
+            if (nq == 0) {
+                if (h0 < G) { scr_m[w * GMAX + h0] = m0; scr_l[w * GMAX + h0] = l0; }
+                if (h1 < G) { scr_m[w * GMAX + h1] = m1; scr_l[w * GMAX + h1] = l1; }
+            }
+        } else {
+            // ---------------------------------------------- FFMA consumer
+            constexpr int EPC = chunk16<T>::n;
+            constexpr int LPT = 32 / P;              // lanes per token
+            constexpr int CPT = D / LPT;             // channels per lane for q.k
+            constexpr int KCH = CPT / EPC;           // 16-byte chunks per lane for q.k
+            constexpr int DPL = D / 32;              // channels per lane for p.v
+            float *qs = ff_q + w * GMAX * D;
+            float *ps = ff_p + w * GMAX * P;
+            for (int e = lane; e < G * D; e += 32) qs[e] = elem<T>::to_f(qb[e]);
+            __syncwarp();
+            float o[GMAX][DPL], m[GMAX], l[GMAX];
+#pragma unroll
+            for (int gg = 0; gg < GMAX; ++gg) {
+                m[gg] = -INFINITY; l[gg] = 0.f;
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) o[gg][x] = 0.f;
+            }
+            const int tk = lane / LPT, sl = lane % LPT;
+            for (; i < lastx; i += NW) {
+                const int s = (int)(i % S);
+                const uint32_t ph = (uint32_t)((i / S) & 1);
+                if (*abort_flag) break;
+                if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
+                    if (lane == 0 && p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                const int nvalid = info[s].nvalid;
+                const unsigned char *kst = ring + (size_t)s * STAGE;
+                const unsigned char *vst = kst + TILE;
+                if (nvalid > 0) {
+                    float acc[GMAX];
+#pragma unroll
+                    for (int gg = 0; gg < GMAX; ++gg) acc[gg] = 0.f;
+#pragma unroll
+                    for (int x = 0; x < KCH; ++x) {
+                        const int chunk = sl * KCH + x;
+                        float f[EPC];
+                        chunk16<T>::unpack(*reinterpret_cast<const uint4 *>(kst + swz128_offset<P>(tk, chunk)), f);
+#pragma unroll
+                        for (int gg = 0; gg < GMAX; ++gg)
+#pragma unroll
+                            for (int e = 0; e < EPC; ++e)
+                                acc[gg] = fmaf(qs[gg * D + chunk * EPC + e], f[e], acc[gg]);
+                    }
+                    const bool valid = tk < nvalid;
+#pragma unroll
+                    for (int gg = 0; gg < GMAX; ++gg) {
+                        if (gg >= G) break;
+                        float a = acc[gg];
+                        if (LPT == 2) a += __shfl_xor_sync(0xffffffffu, a, 1);
+                        const float z = valid ? a * p.scale_log2 : -INFINITY;
+                        float mx = z;
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                        const float nm = fmaxf(m[gg], mx);
+                        const float al = exp2f(m[gg] - nm);
+                        const float pz = exp2f(z - nm);
+                        float sum = sl == 0 ? pz : 0.f;
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                        l[gg] = l[gg] * al + sum;
+                        m[gg] = nm;
+#pragma unroll
+                        for (int x = 0; x < DPL; ++x) o[gg][x] *= al;
+                        if (sl == 0) ps[gg * P + tk] = pz;
+                    }
+                    __syncwarp();
+                    for (int t = 0; t < nvalid; ++t) {
+                        const int byte = lane * DPL * ES;
+                        const unsigned char *vp = vst + swz128_offset<P>(t, byte >> 4) + (byte & 15);
+                        float v[DPL];
+#pragma unroll
+                        for (int x = 0; x < DPL; ++x) v[x] = elem<T>::to_f(reinterpret_cast<const T *>(vp)[x]);
+#pragma unroll
+                        for (int gg = 0; gg < GMAX; ++gg) {
+                            if (gg >= G) break;
+                            const float pw = ps[gg * P + t];
+#pragma unroll
+                            for (int x = 0; x < DPL; ++x) o[gg][x] = fmaf(pw, v[x], o[gg][x]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[s]);
+            }
+#pragma unroll
+            for (int gg = 0; gg < GMAX; ++gg) {
+                if (gg >= G) break;
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) scr_o[(w * GMAX + gg) * D + lane * DPL + x] = o[gg][x];
+                if (lane == 0) { scr_m[w * GMAX + gg] = m[gg]; scr_l[w * GMAX + gg] = l[gg]; }
+            }
+        }
+
+        // --------------------------------------------- merge the consumer warps
+        named_barrier_sync(1, NCT);
+        const bool whole = (g == us) && (s1 == ue);
+        const int slot = u + c;
+        for (int e = ct; e < G * D; e += NCT) {
+            const int hh = e / D, ch = e - hh * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int x = 0; x < NW; ++x) M = fmaxf(M, scr_m[x * GMAX + hh]);
+            float Ls = 0.f, acc = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int x = 0; x < NW; ++x) {
+                    const float f = exp2f(scr_m[x * GMAX + hh] - M);
+                    Ls += scr_l[x * GMAX + hh] * f;
+                    acc += scr_o[(x * GMAX + hh) * D + ch] * f;
+                }
+            }
+            if (whole) {
+                static_cast<T *>(p.out)[((size_t)b * p.Hq + (size_t)h * G + hh) * D + ch] =
+                    elem<T>::from_f(Ls > 0.f ? acc / Ls : 0.f);
+            } else {
+                p.part_o[((size_t)slot * G + hh) * D + ch] = acc;
+                if (ch == 0) {
+                    p.part_ml[((size_t)slot * G + hh) * 2] = M;
+                    p.part_ml[((size_t)slot * G + hh) * 2 + 1] = Ls;
+                }
+            }
+        }
+        if (!whole) {
+            __threadfence();
+            named_barrier_sync(1, NCT);
+            const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
+            if (ct == 0) {
+                const int prev = atomicAdd(&p.counters[u], 1);
+                s_flag = (prev == cl - cf);
+            }
+            named_barrier_sync(1, NCT);
+            if (s_flag) {
+                __threadfence();
+                for (int e = ct; e < G * D; e += NCT) {
+                    const int hh = e / D, ch = e - hh * D;
+                    float M = -INFINITY;
+                    for (int x = cf; x <= cl; ++x) M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(u + x) * G + hh) * 2]));
+                    float Ls = 0.f, acc = 0.f;
+                    if (M != -INFINITY) {
+                        for (int x = cf; x <= cl; ++x) {
+                            const size_t sl = (size_t)(u + x) * G + hh;
+                            const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - M);
+                            Ls += __ldcg(&p.part_ml[sl * 2 + 1]) * f;
+                            acc += __ldcg(&p.part_o[sl * D + ch]) * f;
+                        }
+                    }
+                    static_cast<T *>(p.out)[((size_t)b * p.Hq + (size_t)h * G + hh) * D + ch] =
+                        elem<T>::from_f(Ls > 0.f ? acc / Ls : 0.f);
+                }
+                if (ct == 0) p.counters[u] = 0;
+            }
+        }
+        named_barrier_sync(1, NCT);
+        g = s1;
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+template <typename T, int D, int P, bool MMA, int GMAX>
+static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p0,
+                                 int grid, size_t smem_budget, bool pdl, cudaStream_t stream) {
+    constexpr int NW = 8;
+    constexpr int STAGE = 2 * P * D * (int)sizeof(T);
+    AttnParams p = p0;
+    const size_t fixed = attn_smem_bytes(0, STAGE, NW, GMAX, D, P, MMA, p.B);
+    const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo);
+    int stages = (int)((smem_budget - fixed) / per);
+    if (stages > 32) stages = 32;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
+    p.stages = stages;
+    const size_t smem = attn_smem_bytes(stages, STAGE, NW, GMAX, D, P, MMA, p.B);
+    auto kern = attn_kernel<T, D, P, MMA, GMAX, NW>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 * (NW + 1));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, km, vm, p);
+}
+
+template <typename T, int D, int P>
+static cudaError_t launch_attn_dp(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p,
+                                  int grid, size_t smem_budget, bool pdl, cudaStream_t stream) {
+    if constexpr (sizeof(T) == 2) {
+        // tensor cores when the query group makes q.K a real contraction
+        if (p.G >= 2) return launch_attn_t<T, D, P, true, 8>(km, vm, p, grid, smem_budget, pdl, stream);
+        return launch_attn_t<T, D, P, false, 1>(km, vm, p, grid, smem_budget, pdl, stream);
+    } else {
+        return launch_attn_t<T, D, P, false, 8>(km, vm, p, grid, smem_budget, pdl, stream);
+    }
+}
+
+template <typename T>
+static cudaError_t launch_attn_dt(int D, int P, const CUtensorMap &km, const CUtensorMap &vm,
+                                  const AttnParams &p, int grid, size_t smem_budget, bool pdl,
+                                  cudaStream_t stream) {
+    if (D == 64)
+        return P == 16 ? launch_attn_dp<T, 64, 16>(km, vm, p, grid, smem_budget, pdl, stream)
+                       : launch_attn_dp<T, 64, 32>(km, vm, p, grid, smem_budget, pdl, stream);
+    return P == 16 ? launch_attn_dp<T, 128, 16>(km, vm, p, grid, smem_budget, pdl, stream)
+                   : launch_attn_dp<T, 128, 32>(km, vm, p, grid, smem_budget, pdl, stream);
+}
+
+cudaError_t launch_attention(qasa_dtype dt, int D, int P, const CUtensorMap &km,
+                             const CUtensorMap &vm, const AttnParams &p, int grid,
+                             size_t smem_budget, bool pdl, cudaStream_t stream) {
+    switch (dt) {
+    case QASA_DTYPE_F32: return launch_attn_dt<float>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
+    case QASA_DTYPE_F16: return launch_attn_dt<__half>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
+    default: return launch_attn_dt<__nv_bfloat16>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
+    }
+}
+
+}  // namespace qasa

@@ -1,0 +1,63 @@
+// qasa_launch.h -- kernel parameter blocks and launchers shared by the
+// kernel translation units and the C entry points (host + device visible).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qasa.h"
+
+namespace qasa {
+
+struct AppendParams {
+    void *k_pool;
+    void *v_pool;
+    void *bounds;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int32_t *append_lens;
+    const void *k_new;
+    const void *v_new;
+    int32_t *status;
+    int num_phys, Hkv, P, max_pages, T;
+};
+
+struct SelectParams {
+    const void *bounds;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int32_t *budget;
+    const void *q;
+    int32_t *selected;
+    float *scores_out;
+    int32_t *counters;
+    int32_t *status;
+    int num_phys, Hkv, P, G, Hq, max_pages, max_budget;
+};
+
+struct AttnParams {
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int32_t *budget;
+    const int32_t *selected;
+    const void *q;
+    void *out;
+    float *part_o;     // [(units + C) * G * D]
+    float *part_ml;    // [(units + C) * G * 2]  (running max in log2 units, sum of weights)
+    int32_t *counters; // [units]
+    int32_t *status;
+    int B, Hkv, G, Hq, max_pages, max_budget, num_phys;
+    float scale_log2;
+    int dense;
+    int stages;
+    unsigned long long wait_limit_ns;
+};
+
+cudaError_t launch_append(qasa_dtype dt, int D, const AppendParams &p, int batch, cudaStream_t stream);
+cudaError_t launch_select(qasa_dtype dt, int D, const SelectParams &p, int units, cudaStream_t stream);
+cudaError_t launch_attention(qasa_dtype dt, int D, int P, const CUtensorMap &km, const CUtensorMap &vm,
+                             const AttnParams &p, int grid, size_t smem_budget, bool pdl,
+                             cudaStream_t stream);
+
+}  // namespace qasa

@@ -1,0 +1,285 @@
+"""CUDA path vs CPU oracle on the same seeded inputs (needs a GB300).
+
+Element-by-element at reduced batch (several tiles, ragged tails); sampled
+(sequence, KV head) units at the full sizes the benchmark runs.  Bars:
+page boxes exact; scores within the fp32 summation bound; kept page sets
+identical wherever the boundary scores are not tied (1e-5 relative, widened
+to the fp32 bound); outputs within 2e-3 absolute + 1e-2 relative of the fp64
+oracle (on the GPU's own selection when a tie let the sets differ).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from query_aware_sparse_append_gb300 import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from query_aware_sparse_append_gb300 import build
+    build.build()
+
+
+def qasa():
+    from query_aware_sparse_append_gb300 import binding
+    return binding
+
+
+def run_sparse(case, max_budget=None, budget=None):
+    q = qasa()
+    cfg = case.cfg
+    B = cfg.batch
+    maxp = case.bt.shape[1]
+    bud = case.budget_dev if budget is None else budget
+    if max_budget is None:
+        max_budget = max(2, maxp)
+    scores = torch.full((B, cfg.num_kv_heads, maxp), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, sel = q.sparse_decode_attention(case.cache, case.q_dev, case.bt, case.lens_dev, bud,
+                                         max_budget=max_budget, scores=scores, status=status)
+    torch.cuda.synchronize()
+    return out, sel, scores, int(status.item())
+
+
+def check_units(case, out, sel, scores, units, check_bounds=True):
+    cfg = case.cfg
+    P = cfg.page_size
+    out64 = H.gpu_out64(out, cfg.dtype)
+    sel = sel.cpu().numpy()
+    scores = scores.cpu().numpy()
+    bounds = H.from_torch(case.cache.page_bounds, cfg.dtype) if check_bounds else None
+    n_equal = 0
+    for b, h in units:
+        L = int(case.lens[b])
+        N = -(-L // P)
+        K = case.k64(b, h)
+        lo, hi = oracle.page_bounds(K, P)
+        if check_bounds and N:
+            phys = case.plan.block_table[b, :N]
+            glo = W.widen(bounds[phys, h, 0], cfg.dtype)
+            ghi = W.widen(bounds[phys, h, 1], cfg.dtype)
+            assert np.array_equal(glo, lo) and np.array_equal(ghi, hi), (b, h)
+        q64 = case.q64(b, h)
+        o_s, o_sel, o_out = oracle.decode_unit(q64, K, case.v64(b, h), lo, hi, L, P,
+                                               int(case.budgets[b]))
+        if N == 0:
+            assert np.all(sel[b, h] == -1)
+            assert np.all(out64[b, h * case.G:(h + 1) * case.G] == 0)
+            continue
+        g_s = scores[b, h, :N].astype(np.float64)
+        k_eff = len(o_sel)
+        if k_eff < N:
+            tol = H.score_tolerance(q64, lo, hi)
+            assert np.all(np.abs(g_s - o_s) <= tol), (b, h, np.max(np.abs(g_s - o_s) - tol))
+        same = H.check_selection(sel[b, h], g_s if k_eff < N else None, o_s, o_sel, k_eff,
+                                 H.score_tolerance(q64, lo, hi))
+        ref = o_out if same else oracle.attention(q64, K, case.v64(b, h), L, P,
+                                                  sel[b, h][sel[b, h] >= 0])
+        n_equal += same
+        H.assert_close(out64[b, h * case.G:(h + 1) * case.G], ref, "out b=%d h=%d" % (b, h))
+    return n_equal
+
+
+def all_units(case):
+    return [(b, h) for b in range(case.cfg.batch) for h in range(case.cfg.num_kv_heads)]
+
+
+# ------------------------------------------------------------- reduced sizes
+
+REDUCED = [
+    ("tiny", None, 0), ("tiny", None, 1), ("tiny", None, 2),
+    ("tinyllama", 3, 0), ("tinyllama", 2, 1),
+    ("gpt2_345m", 12, 0), ("gpt2_345m", 8, 2),
+    ("llama_1b3_32k", 1, 0),
+    ("serving_mix", 6, 0), ("serving_mix", 4, 1),
+    ("headline_8k", 3, 0),
+]
+
+
+@pytest.mark.parametrize("name,batch,seed", REDUCED)
+def test_sparse_decode_matches_oracle(name, batch, seed):
+    case = H.make_case(W.CONFIGS[name], seed=seed, batch=batch)
+    out, sel, scores, st = run_sparse(case)
+    assert st == 0
+    check_units(case, out, sel, scores, all_units(case))
+
+
+@pytest.mark.parametrize("permille", W.SERVING_MIX_BUDGETS_PERMILLE)
+def test_serving_mix_budget_sweep(permille):
+    cfg = W.CONFIGS["serving_mix"].with_budget("permille", permille)
+    case = H.make_case(cfg, seed=3, batch=5)
+    out, sel, scores, st = run_sparse(case)
+    assert st == 0
+    check_units(case, out, sel, scores, all_units(case))
+
+
+@pytest.mark.parametrize("name", ["tiny", "tinyllama", "gpt2_345m", "llama_1b3_32k", "serving_mix"])
+def test_dense_matches_oracle_and_full_budget(name):
+    case = H.make_case(W.CONFIGS[name], seed=4, batch=min(3, W.CONFIGS[name].batch))
+    q = qasa()
+    dense = q.dense_decode_attention(case.cache, case.q_dev, case.bt, case.lens_dev)
+    full = torch.full_like(case.budget_dev, 1 << 20)
+    out, sel, scores, st = run_sparse(case, budget=full)
+    torch.cuda.synchronize()
+    assert st == 0
+    d64 = H.gpu_out64(dense, case.cfg.dtype)
+    s64 = H.gpu_out64(out, case.cfg.dtype)
+    P, G = case.cfg.page_size, case.G
+    for b, h in all_units(case):
+        L = int(case.lens[b])
+        ref = oracle.dense_attention(case.q64(b, h), case.k64(b, h), case.v64(b, h), L, P)
+        H.assert_close(d64[b, h * G:(h + 1) * G], ref, "dense")
+        H.assert_close(s64[b, h * G:(h + 1) * G], ref, "full budget")
+        N = -(-L // P)
+        assert np.array_equal(sel[b, h, :N].cpu().numpy(), np.arange(N))
+
+
+def test_physical_permutation_changes_nothing():
+    cfg = W.CONFIGS["serving_mix"]
+    a = H.make_case(cfg, seed=5, batch=4, shuffle=True)
+    b = H.make_case(cfg, seed=5, batch=4, shuffle=False)
+    oa, sa, _, _ = run_sparse(a)
+    ob, sb, _, _ = run_sparse(b)
+    assert torch.equal(sa, sb)
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+
+
+@pytest.mark.parametrize("chunks", [[1] * 40 + [10 ** 6], [7, 9, 1, 33, 10 ** 6], [16, 15, 17, 10 ** 6]])
+def test_chunked_appends_give_the_same_boxes_and_result(chunks):
+    cfg = W.CONFIGS["gpt2_345m"]
+    one = H.make_case(cfg, seed=6, batch=4)
+    many = H.make_case(cfg, seed=6, batch=4, append_chunks=chunks)
+    assert torch.equal(one.cache.page_bounds.view(torch.int16), many.cache.page_bounds.view(torch.int16))
+    o1, s1, _, _ = run_sparse(one)
+    o2, s2, _, _ = run_sparse(many)
+    assert torch.equal(s1, s2) and torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    out, sel, scores, st = run_sparse(many)
+    check_units(many, out, sel, scores, all_units(many))
+
+
+def test_recycled_pages_start_fresh_boxes():
+    # sequence 0's first page is overwritten from slot 0 by foreign keys, then
+    # refilled from slot 0 with its own keys: the box must be its own again
+    cfg = W.CONFIGS["tinyllama"]
+    case = H.make_case(cfg, seed=7, batch=2)
+    q = qasa()
+    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+    big = torch.full((1, 16, cfg.num_kv_heads, cfg.head_dim), 50.0, dtype=torch.float16, device="cuda")
+    bt0 = case.bt[:1].contiguous()
+    q.kv_append(case.cache, bt0, zero, big, big)
+    L = int(case.lens[0])
+    kn = H.to_torch(case.seqs[0].k[None], "f16").cuda()
+    vn = H.to_torch(case.seqs[0].v[None], "f16").cuda()
+    q.kv_append(case.cache, bt0, zero, kn, vn)
+    assert kn.shape[1] == L
+    out, sel, scores, st = run_sparse(case)
+    check_units(case, out, sel, scores, all_units(case))
+
+
+def test_decode_step_append_then_attend():
+    # one decode step: append a token per sequence (T=1), then attend with it
+    cfg = W.CONFIGS["serving_mix"]
+    case = H.make_case(cfg, seed=8, batch=6, reserve_tokens=3)
+    q = qasa()
+    for step in range(3):
+        kn, vn = [], []
+        for b in range(cfg.batch):
+            k1, v1 = W.append_tokens(cfg, b, 3, seed=8)
+            kn.append(k1[step:step + 1])
+            vn.append(v1[step:step + 1])
+            case.seqs[b].k = np.concatenate([case.seqs[b].k, k1[step:step + 1]])
+            case.seqs[b].v = np.concatenate([case.seqs[b].v, v1[step:step + 1]])
+        q.kv_append(case.cache, case.bt, case.lens_dev, H.to_torch(np.stack(kn), "f16").cuda(),
+                    H.to_torch(np.stack(vn), "f16").cuda())
+        case.lens = case.lens + 1
+        case.lens_dev += 1
+        case.budgets = W.budgets(cfg, case.lens)
+        case.budget_dev = torch.from_numpy(case.budgets).cuda()
+        out, sel, scores, st = run_sparse(case)
+        assert st == 0
+        check_units(case, out, sel, scores, all_units(case))
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_edge_lengths_and_budgets():
+    cfg = W.CONFIGS["tinyllama"].with_batch(8)
+    lens = np.array([0, 1, 15, 16, 17, 33, 4096, 100], dtype=np.int32)
+    budgets = np.array([4, 1, 1, 1, 1, 2, 3, 1000], dtype=np.int32)
+    case = H.make_case(cfg, seed=9, lens=lens, budgets=budgets)
+    out, sel, scores, st = run_sparse(case)
+    assert st == 0
+    check_units(case, out, sel, scores, all_units(case))
+    o = H.gpu_out64(out, "f16")
+    # one token: the output is that token's value row for every query head
+    v = W.widen(case.seqs[1].v[0], "f16")
+    for h in range(cfg.num_kv_heads):
+        assert np.allclose(o[1, h * 8:(h + 1) * 8], v[h][None], atol=1e-3, rtol=0)
+
+
+def test_budget_above_max_budget_is_clamped_and_reported():
+    cfg = W.CONFIGS["tinyllama"]
+    case = H.make_case(cfg, seed=10, batch=2)
+    out, sel, scores, st = run_sparse(case, max_budget=8)
+    assert st & 0x4
+    assert sel.shape[-1] == 8 and bool((sel >= 0).all())
+
+
+def test_bad_block_table_entry_is_skipped_and_reported():
+    cfg = W.CONFIGS["tinyllama"]
+    case = H.make_case(cfg, seed=11, batch=2)
+    case.bt[1, 5] = case.plan.num_phys_pages + 7     # out of range
+    out, sel, scores, st = run_sparse(case)
+    assert st & 0x1
+    assert torch.isfinite(out.float()).all()
+
+
+def test_seq_len_beyond_block_table_is_clamped_and_reported():
+    cfg = W.CONFIGS["tinyllama"]
+    case = H.make_case(cfg, seed=12, batch=2)
+    case.lens_dev[0] = case.bt.shape[1] * cfg.page_size + 5
+    out, sel, scores, st = run_sparse(case)
+    assert st & 0x2
+    assert torch.isfinite(out.float()).all()
+
+
+def test_empty_batch_is_a_no_op():
+    cfg = W.CONFIGS["tinyllama"]
+    case = H.make_case(cfg, seed=13, batch=2)
+    q = qasa()
+    out, sel = q.sparse_decode_attention(case.cache, case.q_dev[:0], case.bt[:0], case.lens_dev[:0],
+                                         case.budget_dev[:0], max_budget=8)
+    assert out.shape[0] == 0
+
+
+# ----------------------------------------------------------- full-size samples
+
+FULL = [("headline_8k", 0), ("serving_mix", 0), ("llama_1b3_32k", 0), ("gpt2_345m", 0),
+        ("tinyllama", 0)]
+
+
+@pytest.mark.parametrize("name,seed", FULL)
+def test_full_size_sampled_units(name, seed):
+    cfg = W.CONFIGS[name]
+    case = H.make_case(cfg, seed=seed, poison=False)
+    out, sel, scores, st = run_sparse(case)
+    assert st == 0
+    rng = np.random.default_rng(seed)
+    units = all_units(case)
+    pick = [units[i] for i in rng.choice(len(units), size=min(8, len(units)), replace=False)]
+    pick += [units[0], units[-1]]
+    check_units(case, out, sel, scores, pick)
+    # properties at every unit: kept count and ascending ids, finite outputs
+    s = sel.cpu().numpy()
+    for b, h in units:
+        N = -(-int(case.lens[b]) // cfg.page_size)
+        k = min(N, max(int(case.budgets[b]), min(N, 2)))
+        row = s[b, h]
+        assert np.all(row[:k] >= 0) and np.all(np.diff(row[:k]) > 0) and np.all(row[k:] == -1)
+    assert torch.isfinite(out.float()).all()
