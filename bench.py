@@ -124,55 +124,134 @@ def profiled_traffic():
 # ------------------------------------------------------------ clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock and the clock-event (throttle) reasons of one GPU
+    during the timed region: NVML read-only queries through ctypes every ~2 ms
+    from a thread (the region can be a few milliseconds long), else nvidia-smi.
+    Nothing here changes any GPU setting."""
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.file = None
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        self.device = device
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.note = None
+        self._stop = None
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+
+    def _open_nvml(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+        except (AttributeError, RuntimeError):
+            pass
+        ok = False
+        if uuid:
+            u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(handle)) == 0
+        if not ok:
+            count = ctypes.c_uint()
+            lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+            if count.value != 1:
+                raise OSError("cannot map the CUDA device to an NVML device")
+            if lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(handle)) != 0:
+                raise OSError("nvmlDeviceGetHandleByIndex failed")
+        self._nvml, self._handle = lib, handle
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+
+    def _poll(self):
+        import ctypes
+        lib, h = self._nvml, self._handle
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if get_reasons(h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            self._stop.wait(0.002)
 
     def __enter__(self):
+        import threading
         try:
-            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+            self._open_nvml()
+        except OSError as e:
+            self.note = "nvml unavailable (%s); nvidia-smi fallback" % e
+            return self._enter_smi()
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._poll, daemon=True)
+        self._thread.start()
+        return self
+
+    def _enter_smi(self):
+        self._file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=self.file, stderr=subprocess.DEVNULL)
+                stdout=self._file, stderr=subprocess.DEVNULL)
         except OSError:
-            self.proc = None
+            self._proc = None
+        time.sleep(1.0)  # first sample lands before the timed region
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(2)
             try:
-                self.proc.wait(timeout=5)
+                self._nvml.nvmlShutdown()
+            except Exception:
+                pass
+        elif getattr(self, "_proc", None) is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
+                self._proc.kill()
+            self._read_smi()
 
-    def summary(self):
-        if self.proc is None or self.file is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.file.flush()
-        with open(self.file.name) as f:
+    def _read_smi(self):
+        self._file.flush()
+        with open(self._file.name) as f:
             rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
-        os.unlink(self.file.name)
+        os.unlink(self._file.name)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm, mx, reasons = [], [], set()
         for r in rows:
             try:
-                sm.append(float(r[0]))
-                mx.append(float(r[1]))
+                self.samples.append(float(r[0]))
+                self.max_mhz = max(self.max_mhz or 0.0, float(r[1]))
             except (ValueError, IndexError):
                 continue
             for name, v in zip(names, r[2:6]):
                 if v.strip().lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                    self.reasons.add(name)
+
+    def summary(self):
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+               "samples": len(self.samples)}
+        if self.note:
+            out["note"] = self.note
+        return out
 
 
 # ------------------------------------------------------------ CPU oracle leg
@@ -229,6 +308,8 @@ def run_reference(args):
         return 0
     from query_aware_sparse_append_gb300 import workloads as W
     cfg = W.CONFIGS[args.config]
+    if args.batch:
+        cfg = cfg.with_batch(args.batch)
     per_step = max(2.0, 30.0 / max(1, args.steps + args.warmup))
     base = oracle_sample(cfg, args.seed, seconds=per_step * (args.steps + args.warmup))
     v = base["value"]
@@ -274,6 +355,8 @@ def run_ours(args):
     from query_aware_sparse_append_gb300 import workloads as W
 
     cfg = W.CONFIGS[args.config]
+    if args.batch:
+        cfg = cfg.with_batch(args.batch)
     seed = rank_seed(args.seed, rank)
     wl = paged.load(paged.generate(cfg, seed=seed), device=dev)
     B, Hq, Hkv, d = cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
@@ -299,7 +382,7 @@ def run_ours(args):
     # ---- timed region: K fused decode steps, L2 flushed before each
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         barrier(dev)
         torch.cuda.synchronize(dev)
         for i in range(args.steps):
@@ -425,6 +508,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="headline_8k")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline (0 to skip)")

@@ -14,7 +14,8 @@
 // takes the contiguous range [c*T/C, (c+1)*T/C).  A range covers whole units
 // (written straight to `out`) and at most two partial units at its ends,
 // whose partial (m, l, o) go to workspace slot (unit + c); the CTA that
-// finishes a unit last (atomic ticket, no waiting) merges its partials.
+// finishes a unit last (atomic ticket counting the unit's pages, no waiting)
+// merges its partials.
 //
 // Inside a CTA: warp 0 is the producer.  It turns kept page ids into physical
 // tiles through the block table and issues one tiled TMA box per 128 bytes of
@@ -499,10 +500,13 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         if (!whole) {
             __threadfence();
             named_barrier_sync(1, NCT);
+            // the ticket counts pages, so CTAs whose range is empty (grid larger
+            // than the number of kept pages) cannot leave it short
             const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
             if (ct == 0) {
-                const int prev = atomicAdd(&p.counters[u], 1);
-                s_flag = (prev == cl - cf);
+                const int npg = (int)(s1 - g);
+                const int prev = atomicAdd(&p.counters[u], npg);
+                s_flag = (prev + npg == cnt);
             }
             named_barrier_sync(1, NCT);
             if (s_flag) {
@@ -510,10 +514,14 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 for (int e = ct; e < G * D; e += NCT) {
                     const int hh = e / D, ch = e - hh * D;
                     float M = -INFINITY;
-                    for (int x = cf; x <= cl; ++x) M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(u + x) * G + hh) * 2]));
+                    for (int x = cf; x <= cl; ++x) {
+                        if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;   // empty range
+                        M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(u + x) * G + hh) * 2]));
+                    }
                     float Ls = 0.f, acc = 0.f;
                     if (M != -INFINITY) {
                         for (int x = cf; x <= cl; ++x) {
+                            if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;
                             const size_t sl = (size_t)(u + x) * G + hh;
                             const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - M);
                             Ls += __ldcg(&p.part_ml[sl * 2 + 1]) * f;

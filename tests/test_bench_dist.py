@@ -1,0 +1,77 @@
+"""Host logic of the multi-GPU benchmark on CPU: world_size-2 gloo ranks.
+
+Every rank decodes its own batch (weak scaling): distinct seeds, no data-path
+collective; the only collective is the max over ranks of the step time.
+"""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from query_aware_sparse_append_gb300 import workloads as W
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        r, lr, w = bench.dist_env()
+        local = 1.5 + 2.0 * rank               # rank 1 is the slow one
+        bench.barrier()
+        got = bench.max_over_ranks(local)
+        seed = bench.rank_seed(7, r)
+        lens = W.seq_lens(W.CONFIGS["serving_mix"], seed)
+        results[rank] = (r, w, got, seed, int(lens.sum()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_max_time_and_distinct_batches():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank_main, args=(r, 2, port, results)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(results)
+    assert res[0][2] == res[1][2] == 3.5
+    assert res[0][1] == res[1][1] == 2
+    assert res[0][3] != res[1][3] and res[0][4] != res[1][4]
+
+
+def test_single_process_max_is_identity():
+    assert bench.max_over_ranks(2.25) == 2.25
+
+
+def test_algorithmic_bytes_of_the_headline_case():
+    cfg = W.CONFIGS["headline_8k"]
+    lens = W.seq_lens(cfg, 0)
+    sel, att, dense = bench.algorithmic_bytes(cfg, lens, W.budgets(cfg, lens))
+    # 128 sequences x 4 KV heads: 512 pages of 512-byte boxes; 64 kept 8 KiB page pairs
+    units = 128 * 4
+    assert sel == units * (512 * 512 + 8 * 128 * 2 + 4 * 512 + 4 * 64)
+    assert att == units * (64 * 2 * 16 * 128 * 2 + 2 * 8 * 128 * 2 + 8 * 64)
+    assert abs((sel + att) / 1e6 - 407.2) < 0.1
+    assert dense > 5 * att
+
+
+def test_bench_rejects_short_warmup():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
