@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "qasa_launch.h"
@@ -99,23 +100,41 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 2-D view of a KV pool: rows = (page, head, slot), columns = head_dim; one
-// TMA box = 128 bytes of columns x page_size rows, 128-byte swizzle.
-qasa_status pool_tensor_map(CUtensorMap *map, void *base, const qasa_kv_cache *c) {
+// Views of a KV pool for TMA, 128-byte swizzle in both.
+//  3-D (one box per (page, head) tile): dim0 = 128 bytes of head dim, dim1 =
+//      rows (page, head, slot) with stride head_dim*es, dim2 = the 128-byte
+//      column blocks with stride 128 B; box = (128 B, page_size, all blocks), so
+//      the tile lands as [block][slot][128 B].
+//  2-D fallback: rows x head_dim, box = 128 bytes x page_size, one box per
+//      column block.
+qasa_status pool_tensor_map(CUtensorMap *map, void *base, const qasa_kv_cache *c, bool three_d) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return QASA_ERR_DRIVER;
     const size_t es = elem_size(c->dtype);
     const CUtensorMapDataType t = c->dtype == QASA_DTYPE_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                   : c->dtype == QASA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    cuuint64_t dims[2] = {(cuuint64_t)c->head_dim,
-                          (cuuint64_t)c->num_phys_pages * c->num_kv_heads * c->page_size};
-    cuuint64_t strides[1] = {(cuuint64_t)c->head_dim * es};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)c->page_size};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, t, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t rows = (cuuint64_t)c->num_phys_pages * c->num_kv_heads * c->page_size;
+    const cuuint32_t boxw = (cuuint32_t)(128 / es);
+    const cuuint32_t nsub = (cuuint32_t)(c->head_dim * es / 128);
+    CUresult r;
+    if (three_d) {
+        cuuint64_t dims[3] = {boxw, rows, nsub};
+        cuuint64_t strides[2] = {(cuuint64_t)c->head_dim * es, 128};
+        cuuint32_t box[3] = {boxw, (cuuint32_t)c->page_size, nsub};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(map, t, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[2] = {(cuuint64_t)c->head_dim, rows};
+        cuuint64_t strides[1] = {(cuuint64_t)c->head_dim * es};
+        cuuint32_t box[2] = {boxw, (cuuint32_t)c->page_size};
+        cuuint32_t estr[2] = {1, 1};
+        r = enc(map, t, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS ? QASA_OK : QASA_ERR_DRIVER;
 }
 
@@ -156,10 +175,24 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     if (!workspace) return QASA_ERR_WORKSPACE;
     if (ws_bytes < w.total || !aligned16(workspace)) return QASA_ERR_WORKSPACE;
     CUtensorMap km, vm;
-    qasa_status st = pool_tensor_map(&km, cache->k_pool, cache);
-    if (st != QASA_OK) return st;
-    st = pool_tensor_map(&vm, cache->v_pool, cache);
-    if (st != QASA_OK) return st;
+    int one_box = 1;
+    if (pool_tensor_map(&km, cache->k_pool, cache, true) != QASA_OK ||
+        pool_tensor_map(&vm, cache->v_pool, cache, true) != QASA_OK) {
+        one_box = 0;
+        qasa_status st = pool_tensor_map(&km, cache->k_pool, cache, false);
+        if (st != QASA_OK) return st;
+        st = pool_tensor_map(&vm, cache->v_pool, cache, false);
+        if (st != QASA_OK) return st;
+    }
+    if (const char *force = std::getenv("QASA_TMA_2D")) {   // diagnostic: force the 2-D path
+        if (force[0] == '1') {
+            one_box = 0;
+            qasa_status st = pool_tensor_map(&km, cache->k_pool, cache, false);
+            if (st != QASA_OK) return st;
+            st = pool_tensor_map(&vm, cache->v_pool, cache, false);
+            if (st != QASA_OK) return st;
+        }
+    }
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     if (dense && cudaMemsetAsync(ws + w.counters, 0, (size_t)batch * cache->num_kv_heads * 4, stream) != cudaSuccess)
         return QASA_ERR_CUDA;
@@ -184,6 +217,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)cache->head_dim);
     p.scale_log2 = (float)(sc * 1.4426950408889634);
     p.dense = dense ? 1 : 0;
+    p.one_box = one_box;
     p.stages = 0;
     p.wait_limit_ns = kWaitLimitNs;
     size_t budget = smem_optin();

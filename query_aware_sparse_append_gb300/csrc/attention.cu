@@ -46,7 +46,7 @@ size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int
     size_t s = 1024;                                   // alignment slack for the ring
     s += (size_t)stages * stage_bytes;
     s += (size_t)stages * 2 * sizeof(uint64_t);        // full / empty barriers
-    s += (size_t)stages * sizeof(StageInfo);
+    s += (size_t)stages * (sizeof(StageInfo) + sizeof(int));
     s += (size_t)nw * gmax * (D + 2) * sizeof(float);  // combine scratch
     if (!mma) s += (size_t)nw * gmax * (D + P) * sizeof(float);
     s += (size_t)(2 * B + 2) * sizeof(int);            // prefix, lengths
@@ -81,7 +81,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)S * STAGE);
     uint64_t *empty_bar = full_bar + S;
     StageInfo *info = reinterpret_cast<StageInfo *>(empty_bar + S);
-    float *scr_o = reinterpret_cast<float *>(info + S);           // [NW][GMAX][D]
+    int *last_ph = reinterpret_cast<int *>(info + S);             // [S] phase of the last copy
+    float *scr_o = reinterpret_cast<float *>(last_ph + S);        // [NW][GMAX][D]
     float *scr_m = scr_o + NW * GMAX * D;                          // [NW][GMAX]
     float *scr_l = scr_m + NW * GMAX;                              // [NW][GMAX]
     float *ff_q = scr_l + NW * GMAX;                               // FFMA only: [NW][GMAX][D]
@@ -96,22 +97,25 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     const int C = gridDim.x, c = blockIdx.x;
     const int Hkv = p.Hkv, G = p.G;
 
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
+    // warp 0 sets up the stage barriers while the other warps start the scan
+    if (warp == 0) {
+        for (int s = lane; s < S; s += 32) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
+            last_ph[s] = -1;
         }
-        s_abort = 0;
+        if (lane == 0) s_abort = 0;
         fence_barrier_init();
+        if (lane == 0) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+        }
     }
-    if (tid == 32) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-    }
-    // per-sequence kept counts (same rule as the selection kernel) and their prefix
+    // per-sequence kept counts (the selection kernel's rule) and their prefix
+    int any_empty = 0;
     {
-        int carry = 0;
         __shared__ int s_wsum[32];
+        int carry = 0;
         for (int base = 0; base < p.B; base += blockDim.x) {
             const int b = base + tid;
             int cnt = 0;
@@ -120,6 +124,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 const int N = (L + P - 1) / P;
                 cnt = p.dense ? N : kept_pages(N, p.budget[b], p.max_budget, nullptr, false);
                 lens[b] = L;
+                any_empty |= (cnt == 0);
             }
             int incl = cnt;
 #pragma unroll
@@ -129,27 +134,31 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
             if (lane == 31) s_wsum[warp] = incl;
             __syncthreads();
-            int wbase = 0;
-            for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
-            int total = 0;
-            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += s_wsum[w];
+            int wbase = 0, total = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+                const int v = s_wsum[w];
+                wbase += w < warp ? v : 0;
+                total += v;
+            }
             if (b < p.B) prefix[b] = carry + wbase + incl - cnt;
             carry += total;
             __syncthreads();
         }
         if (tid == 0) prefix[p.B] = carry;
+        any_empty = __syncthreads_or(any_empty);
     }
-    __syncthreads();
     const long long Ttot = (long long)Hkv * prefix[p.B];
     const long long g0 = range_start(c, C, Ttot), g1 = range_start(c + 1, C, Ttot);
 
     // sequences with no pages: zero their outputs (unit u handled by CTA u % C)
-    for (int b = 0; b < p.B; ++b) {
-        if (prefix[b + 1] != prefix[b]) continue;
-        for (int h = 0; h < Hkv; ++h) {
-            if ((b * Hkv + h) % C != c) continue;
-            T *o = static_cast<T *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
-            for (int i = tid; i < G * D; i += blockDim.x) o[i] = elem<T>::from_f(0.f);
+    if (any_empty) {
+        for (int b = 0; b < p.B; ++b) {
+            if (prefix[b + 1] != prefix[b]) continue;
+            for (int h = 0; h < Hkv; ++h) {
+                if ((b * Hkv + h) % C != c) continue;
+                T *o = static_cast<T *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+                for (int i = tid; i < G * D; i += blockDim.x) o[i] = elem<T>::from_f(0.f);
+            }
         }
     }
 
@@ -172,14 +181,20 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        long long issued_hi = g0;   // pages [g0, issued_hi) had their copies issued
-        for (long long base = g0; base < g1 && !*abort_flag; base += 32) {
-            const long long g = base + lane;
+        // Pages are handled in batches of WB <= min(32, S): the lanes resolve one
+        // page each (kept id -> block table -> tile row), then every lane issues
+        // its own page's two TMA boxes as soon as its stage is free, so up to 32
+        // copies leave per warp instruction instead of one.
+        const int WB = S < 32 ? S : 32;
+        uint32_t stage0 = 0, phase0 = 0;     // stage and phase of the batch's first page
+        bool aborted = false;
+        for (long long base = g0; base < g1 && !aborted; base += WB) {
+            const int nb = (int)min((long long)WB, g1 - base);
             int nvalid = 0, row = 0, page = -1;
-            if (g < g1) {
+            if (lane < nb) {
                 int b, h, j, cnt;
                 long long us;
-                locate(g, b, h, j, us, cnt);
+                locate(base + lane, b, h, j, us, cnt);
                 const int L = lens[b];
                 const int N = (L + P - 1) / P;
                 page = p.dense ? j : p.selected[((size_t)b * Hkv + h) * p.max_budget + j];
@@ -195,49 +210,60 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     }
                 }
             }
-            const int n = (int)min((long long)32, g1 - base);
-            for (int i = 0; i < n; ++i) {
-                const int nv = __shfl_sync(0xffffffffu, nvalid, i);
-                const int rw = __shfl_sync(0xffffffffu, row, i);
-                const int pg = __shfl_sync(0xffffffffu, page, i);
-                if (lane == 0 && !*abort_flag) {
-                    const long long idx = base + i - g0;
-                    const int s = (int)(idx % S);
-                    const uint32_t ph = (uint32_t)((idx / S) & 1);
-                    if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, p.wait_limit_ns)) {
+            uint32_t s_l = stage0 + lane, ph_l = phase0;
+            if (s_l >= (uint32_t)S) { s_l -= S; ph_l ^= 1u; }
+            bool pending = lane < nb;
+            uint64_t t_begin = 0;
+            for (int spin = 0;; ++spin) {
+                const bool any = __any_sync(0xffffffffu, pending);
+                int stop = 0;
+                if (lane == 0 && any && (spin & 63) == 63) {
+                    const uint64_t now = global_timer_ns();
+                    if (t_begin == 0) t_begin = now;
+                    else if (now - t_begin > p.wait_limit_ns || *abort_flag) stop = 1;
+                }
+                stop = __shfl_sync(0xffffffffu, stop, 0);
+                if (!any) break;
+                if (stop) {
+                    if (lane == 0) {
                         if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
                         *abort_flag = 1;
-                    } else {
-                        info[s].page = pg;
-                        info[s].nvalid = nv;
-                        unsigned char *st = ring + (size_t)s * STAGE;
-                        if (nv > 0) {
-                            mbar_arrive_expect_tx(&full_bar[s], STAGE);
-#pragma unroll
-                            for (int x = 0; x < NSUB; ++x) {
-                                tma_load_2d(st + x * P * 128, &kmap, &full_bar[s], x * BOXW, rw);
-                                tma_load_2d(st + TILE + x * P * 128, &vmap, &full_bar[s], x * BOXW, rw);
-                            }
-                        } else {
-                            mbar_arrive(&full_bar[s]);
-                        }
-                        issued_hi = base + i + 1;
                     }
-                }
-                __syncwarp();
-            }
-        }
-        // drain: wait until every copy this CTA issued has landed (bounded)
-        if (lane == 0) {
-            const long long nissued = issued_hi - g0;
-            for (long long idx = (nissued > S ? nissued - S : 0); idx < nissued; ++idx) {
-                const int s = (int)(idx % S);
-                const uint32_t ph = (uint32_t)((idx / S) & 1);
-                if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
-                    if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                    aborted = true;
                     break;
                 }
+                if (pending && mbar_test_wait(&empty_bar[s_l], ph_l ^ 1u)) {
+                    info[s_l].page = page;
+                    info[s_l].nvalid = nvalid;
+                    unsigned char *st = ring + (size_t)s_l * STAGE;
+                    if (nvalid > 0) {
+                        mbar_arrive_expect_tx(&full_bar[s_l], STAGE);
+                        if (p.one_box) {
+                            tma_load_3d(st, &kmap, &full_bar[s_l], 0, row, 0);
+                            tma_load_3d(st + TILE, &vmap, &full_bar[s_l], 0, row, 0);
+                        } else {
+#pragma unroll
+                            for (int x = 0; x < NSUB; ++x) {
+                                tma_load_2d(st + x * P * 128, &kmap, &full_bar[s_l], x * BOXW, row);
+                                tma_load_2d(st + TILE + x * P * 128, &vmap, &full_bar[s_l], x * BOXW, row);
+                            }
+                        }
+                        last_ph[s_l] = (int)ph_l;
+                    } else {
+                        mbar_arrive(&full_bar[s_l]);
+                    }
+                    pending = false;
+                }
             }
+            stage0 += nb;
+            if (stage0 >= (uint32_t)S) { stage0 -= S; phase0 ^= 1u; }
+        }
+        // drain: the copies this CTA issued must land before it exits (bounded)
+        __syncwarp();
+        for (int s = lane; s < S; s += 32) {
+            const int ph = last_ph[s];
+            if (ph >= 0 && !mbar_wait_bounded(&full_bar[s], (uint32_t)ph, p.wait_limit_ns) && p.status)
+                atomicOr(p.status, QASA_DEVERR_TIMEOUT);
         }
         return;
     }
@@ -255,9 +281,12 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         const int u = b * Hkv + h;
         const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
 
-        // first flattened offset in [g - g0, s1 - g0) that belongs to this warp
-        const long long first = g - g0, lastx = s1 - g0;
-        long long i = first + ((w - first % NW) % NW + NW) % NW;
+        // first flattened offset in [g - g0, s1 - g0) that belongs to this warp,
+        // and its ring stage / phase (then advanced incrementally)
+        const int first = (int)(g - g0), lastx = (int)(s1 - g0);
+        int i = first + ((w - first % NW) % NW + NW) % NW;
+        int s = i % S;
+        uint32_t ph = (uint32_t)((i / S) & 1);
 
         if constexpr (MMA) {
             const int cq = lane & 3, nq = lane >> 2;
@@ -276,9 +305,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
             float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-            for (; i < lastx; i += NW) {
-                const int s = (int)(i % S);
-                const uint32_t ph = (uint32_t)((i / S) & 1);
+            for (; i < lastx; i += NW, s += NW) {
+                while (s >= S) { s -= S; ph ^= 1u; }
                 if (*abort_flag) break;
                 if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
                     if (lane == 0 && p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
@@ -391,9 +419,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 for (int x = 0; x < DPL; ++x) o[gg][x] = 0.f;
             }
             const int tk = lane / LPT, sl = lane % LPT;
-            for (; i < lastx; i += NW) {
-                const int s = (int)(i % S);
-                const uint32_t ph = (uint32_t)((i / S) & 1);
+            for (; i < lastx; i += NW, s += NW) {
+                while (s >= S) { s -= S; ph ^= 1u; }
                 if (*abort_flag) break;
                 if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
                     if (lane == 0 && p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
@@ -548,7 +575,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     constexpr int STAGE = 2 * P * D * (int)sizeof(T);
     AttnParams p = p0;
     const size_t fixed = attn_smem_bytes(0, STAGE, NW, GMAX, D, P, MMA, p.B);
-    const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo);
+    const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int);
     int stages = (int)((smem_budget - fixed) / per);
     if (stages > 32) stages = 32;
     if (stages < 2) return cudaErrorInvalidConfiguration;

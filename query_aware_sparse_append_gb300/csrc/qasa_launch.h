@@ -50,6 +50,7 @@ struct AttnParams {
     int B, Hkv, G, Hq, max_pages, max_budget, num_phys;
     float scale_log2;
     int dense;
+    int one_box;       // 1: one 3-D TMA box per K/V tile; 0: one 2-D box per 128 bytes of head dim
     int stages;
     unsigned long long wait_limit_ns;
 };

@@ -184,8 +184,8 @@ def test_recycled_pages_start_fresh_boxes():
 
 def test_decode_step_append_then_attend():
     # one decode step: append a token per sequence (T=1), then attend with it
-    cfg = W.CONFIGS["serving_mix"]
-    case = H.make_case(cfg, seed=8, batch=6, reserve_tokens=3)
+    case = H.make_case(W.CONFIGS["serving_mix"], seed=8, batch=6, reserve_tokens=3)
+    cfg = case.cfg
     q = qasa()
     for step in range(3):
         kn, vn = [], []
