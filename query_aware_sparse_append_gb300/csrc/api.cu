@@ -219,6 +219,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     p.dense = dense ? 1 : 0;
     p.one_box = one_box;
     p.stages = 0;
+    p.consumers = 0;
     p.wait_limit_ns = kWaitLimitNs;
     size_t budget = smem_optin();
     if (budget == 0) return QASA_ERR_CUDA;

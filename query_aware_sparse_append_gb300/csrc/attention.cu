@@ -76,6 +76,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
 
     extern __shared__ unsigned char smem_raw[];
     const int S = p.stages;
+    const int NWK = p.consumers;   // working consumer warps (<= NW, divides S)
     unsigned char *ring = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)S * STAGE);
@@ -281,10 +282,15 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         const int u = b * Hkv + h;
         const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
 
-        // first flattened offset in [g - g0, s1 - g0) that belongs to this warp,
-        // and its ring stage / phase (then advanced incrementally)
-        const int first = (int)(g - g0), lastx = (int)(s1 - g0);
-        int i = first + ((w - first % NW) % NW + NW) % NW;
+        // Page i of the CTA range goes to consumer warp i % NWK and ring stage
+        // i % S.  S is a multiple of NWK, so every stage always belongs to the
+        // same warp, which consumes its rounds in order: a parity wait on a
+        // stage can then never alias with a fill two phases behind (copies
+        // complete out of order, so a stage shared by several warps could be
+        // observed "full" while an older fill into it is still in flight).
+        const int first = (int)(g - g0);
+        const int lastx = w < NWK ? (int)(s1 - g0) : first;
+        int i = first + ((w - first % NWK) % NWK + NWK) % NWK;
         int s = i % S;
         uint32_t ph = (uint32_t)((i / S) & 1);
 
@@ -305,7 +311,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
             float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-            for (; i < lastx; i += NW, s += NW) {
+            for (; i < lastx; i += NWK, s += NWK) {
                 while (s >= S) { s -= S; ph ^= 1u; }
                 if (*abort_flag) break;
                 if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
@@ -419,7 +425,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 for (int x = 0; x < DPL; ++x) o[gg][x] = 0.f;
             }
             const int tk = lane / LPT, sl = lane % LPT;
-            for (; i < lastx; i += NW, s += NW) {
+            for (; i < lastx; i += NWK, s += NWK) {
                 while (s >= S) { s -= S; ph ^= 1u; }
                 if (*abort_flag) break;
                 if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_limit_ns)) {
@@ -579,7 +585,10 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     int stages = (int)((smem_budget - fixed) / per);
     if (stages > 32) stages = 32;
     if (stages < 2) return cudaErrorInvalidConfiguration;
+    const int consumers = stages < NW ? stages : NW;
+    stages = stages / consumers * consumers;    // each stage owned by one consumer warp
     p.stages = stages;
+    p.consumers = consumers;
     const size_t smem = attn_smem_bytes(stages, STAGE, NW, GMAX, D, P, MMA, p.B);
     auto kern = attn_kernel<T, D, P, MMA, GMAX, NW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

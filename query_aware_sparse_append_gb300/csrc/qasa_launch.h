@@ -51,7 +51,8 @@ struct AttnParams {
     float scale_log2;
     int dense;
     int one_box;       // 1: one 3-D TMA box per K/V tile; 0: one 2-D box per 128 bytes of head dim
-    int stages;
+    int stages;        // ring depth, a multiple of `consumers`
+    int consumers;     // consumer warps that take pages (<= the compiled count)
     unsigned long long wait_limit_ns;
 };
 
