@@ -83,12 +83,12 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     uint64_t *empty_bar = full_bar + S;
     StageInfo *info = reinterpret_cast<StageInfo *>(empty_bar + S);
     int *last_ph = reinterpret_cast<int *>(info + S);             // [S] phase of the last copy
-    float *scr_o = reinterpret_cast<float *>(last_ph + S);        // [NW][GMAX][D]
-    float *scr_m = scr_o + NW * GMAX * D;                          // [NW][GMAX]
-    float *scr_l = scr_m + NW * GMAX;                              // [NW][GMAX]
-    float *ff_q = scr_l + NW * GMAX;                               // FFMA only: [NW][GMAX][D]
-    float *ff_p = ff_q + (MMA ? 0 : NW * GMAX * D);                // FFMA only: [NW][GMAX][P]
-    int *prefix = reinterpret_cast<int *>(ff_p + (MMA ? 0 : NW * GMAX * P));   // [B + 1]
+    float *scr_o = reinterpret_cast<float *>(last_ph + S);        // [NWK][GMAX][D]
+    float *scr_m = scr_o + NWK * GMAX * D;                         // [NWK][GMAX]
+    float *scr_l = scr_m + NWK * GMAX;                             // [NWK][GMAX]
+    float *ff_q = scr_l + NWK * GMAX;                              // FFMA only: [NWK][GMAX][D]
+    float *ff_p = ff_q + (MMA ? 0 : NWK * GMAX * D);               // FFMA only: [NWK][GMAX][P]
+    int *prefix = reinterpret_cast<int *>(ff_p + (MMA ? 0 : NWK * GMAX * P));  // [B + 1]
     int *lens = prefix + (p.B + 1);                                // [B]
     __shared__ int s_flag;       // last-arriver flag
     __shared__ int s_abort;      // a bounded wait gave up
@@ -189,28 +189,50 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         const int WB = S < 32 ? S : 32;
         uint32_t stage0 = 0, phase0 = 0;     // stage and phase of the batch's first page
         bool aborted = false;
+        // Lookups are software-pipelined over batches: the kept-id load of batch
+        // k+2 and the block-table load of batch k+1 are in flight while batch k
+        // is issued, so their latency hides behind the ring instead of stalling it.
+        struct Look { int page, phys, b, h; bool active, ok; };
+        auto look_a = [&](long long bb, Look &lk) {      // locate; load the kept id
+            const long long gg = bb + lane;
+            lk.active = lane < WB && gg < g1;
+            lk.ok = false;
+            lk.page = -1; lk.phys = -1; lk.b = 0; lk.h = 0;
+            if (lk.active) {
+                int j, cnt;
+                long long us;
+                locate(gg, lk.b, lk.h, j, us, cnt);
+                lk.page = p.dense ? j : p.selected[((size_t)lk.b * Hkv + lk.h) * p.max_budget + j];
+            }
+        };
+        auto look_b = [&](Look &lk) {                    // check the id; load the block-table entry
+            if (!lk.active) return;
+            const int N = (lens[lk.b] + P - 1) / P;
+            if (lk.page < 0 || lk.page >= N) {
+                if (p.status) atomicOr(p.status, QASA_DEVERR_SELECTED);
+                return;
+            }
+            lk.ok = true;
+            lk.phys = p.block_table[(size_t)lk.b * p.max_pages + lk.page];
+        };
+        Look la, lb, lc;
+        look_a(g0, la);
+        look_b(la);
+        look_a(g0 + WB, lb);
         for (long long base = g0; base < g1 && !aborted; base += WB) {
             const int nb = (int)min((long long)WB, g1 - base);
-            int nvalid = 0, row = 0, page = -1;
-            if (lane < nb) {
-                int b, h, j, cnt;
-                long long us;
-                locate(base + lane, b, h, j, us, cnt);
-                const int L = lens[b];
-                const int N = (L + P - 1) / P;
-                page = p.dense ? j : p.selected[((size_t)b * Hkv + h) * p.max_budget + j];
-                if (page < 0 || page >= N) {
-                    if (p.status) atomicOr(p.status, QASA_DEVERR_SELECTED);
+            int nvalid = 0, row = 0;
+            const int page = la.page;
+            if (la.active && la.ok) {                    // check the physical page
+                if (la.phys < 0 || la.phys >= p.num_phys) {
+                    if (p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
                 } else {
-                    const int phys = p.block_table[(size_t)b * p.max_pages + page];
-                    if (phys < 0 || phys >= p.num_phys) {
-                        if (p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
-                    } else {
-                        nvalid = min(P, L - page * P);
-                        row = (int)(((long long)phys * Hkv + h) * P);
-                    }
+                    nvalid = min(P, lens[la.b] - page * P);
+                    row = (int)(((long long)la.phys * Hkv + la.h) * P);
                 }
             }
+            look_b(lb);
+            look_a(base + 2 * (long long)WB, lc);
             uint32_t s_l = stage0 + lane, ph_l = phase0;
             if (s_l >= (uint32_t)S) { s_l -= S; ph_l ^= 1u; }
             bool pending = lane < nb;
@@ -258,6 +280,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
             stage0 += nb;
             if (stage0 >= (uint32_t)S) { stage0 -= S; phase0 ^= 1u; }
+            la = lb;
+            lb = lc;
         }
         // drain: the copies this CTA issued must land before it exits (bounded)
         __syncwarp();
@@ -272,6 +296,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     // ---------------------------------------------------------------- consumers
     const int w = warp - 1;
     const int ct = tid - 32;
+    const bool working = w < NWK;
     long long g = g0;
     while (g < g1) {
         int b, h, j0, cnt;
@@ -289,7 +314,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         // complete out of order, so a stage shared by several warps could be
         // observed "full" while an older fill into it is still in flight).
         const int first = (int)(g - g0);
-        const int lastx = w < NWK ? (int)(s1 - g0) : first;
+        const int lastx = working ? (int)(s1 - g0) : first;
         int i = first + ((w - first % NWK) % NWK + NWK) % NWK;
         int s = i % S;
         uint32_t ph = (uint32_t)((i / S) & 1);
@@ -393,6 +418,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 const int ch = mt * 16 + nq;
+                if (!working) break;
                 if (h0 < G) {
                     scr_o[(w * GMAX + h0) * D + ch] = o[mt][0];
                     scr_o[(w * GMAX + h0) * D + ch + 8] = o[mt][2];
@@ -402,7 +428,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     scr_o[(w * GMAX + h1) * D + ch + 8] = o[mt][3];
                 }
             }
-            if (nq == 0) {
+            if (nq == 0 && working) {
                 if (h0 < G) { scr_m[w * GMAX + h0] = m0; scr_l[w * GMAX + h0] = l0; }
                 if (h1 < G) { scr_m[w * GMAX + h1] = m1; scr_l[w * GMAX + h1] = l1; }
             }
@@ -413,9 +439,10 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             constexpr int CPT = D / LPT;             // channels per lane for q.k
             constexpr int KCH = CPT / EPC;           // 16-byte chunks per lane for q.k
             constexpr int DPL = D / 32;              // channels per lane for p.v
-            float *qs = ff_q + w * GMAX * D;
-            float *ps = ff_p + w * GMAX * P;
-            for (int e = lane; e < G * D; e += 32) qs[e] = elem<T>::to_f(qb[e]);
+            float *qs = ff_q + (working ? w : 0) * GMAX * D;
+            float *ps = ff_p + (working ? w : 0) * GMAX * P;
+            if (working)
+                for (int e = lane; e < G * D; e += 32) qs[e] = elem<T>::to_f(qb[e]);
             __syncwarp();
             float o[GMAX][DPL], m[GMAX], l[GMAX];
 #pragma unroll
@@ -494,7 +521,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
 #pragma unroll
             for (int gg = 0; gg < GMAX; ++gg) {
-                if (gg >= G) break;
+                if (gg >= G || !working) break;
 #pragma unroll
                 for (int x = 0; x < DPL; ++x) scr_o[(w * GMAX + gg) * D + lane * DPL + x] = o[gg][x];
                 if (lane == 0) { scr_m[w * GMAX + gg] = m[gg]; scr_l[w * GMAX + gg] = l[gg]; }
@@ -509,11 +536,10 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             const int hh = e / D, ch = e - hh * D;
             float M = -INFINITY;
 #pragma unroll
-            for (int x = 0; x < NW; ++x) M = fmaxf(M, scr_m[x * GMAX + hh]);
+            for (int x = 0; x < NWK; ++x) M = fmaxf(M, scr_m[x * GMAX + hh]);
             float Ls = 0.f, acc = 0.f;
             if (M != -INFINITY) {
-#pragma unroll
-                for (int x = 0; x < NW; ++x) {
+                for (int x = 0; x < NWK; ++x) {
                     const float f = exp2f(scr_m[x * GMAX + hh] - M);
                     Ls += scr_l[x * GMAX + hh] * f;
                     acc += scr_o[(x * GMAX + hh) * D + ch] * f;
@@ -531,19 +557,21 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
         }
         if (!whole) {
-            __threadfence();
+            // publish the partial: the barrier orders every consumer's stores before
+            // thread 0's device-scope fence, which releases them with the ticket.
+            // The ticket counts pages, so CTAs whose range is empty (grid larger
+            // than the number of kept pages) cannot leave it short.
             named_barrier_sync(1, NCT);
-            // the ticket counts pages, so CTAs whose range is empty (grid larger
-            // than the number of kept pages) cannot leave it short
             const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
             if (ct == 0) {
+                __threadfence();
                 const int npg = (int)(s1 - g);
                 const int prev = atomicAdd(&p.counters[u], npg);
+                __threadfence();
                 s_flag = (prev + npg == cnt);
             }
             named_barrier_sync(1, NCT);
             if (s_flag) {
-                __threadfence();
                 for (int e = ct; e < G * D; e += NCT) {
                     const int hh = e / D, ch = e - hh * D;
                     float M = -INFINITY;
@@ -580,16 +608,25 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     constexpr int NW = 8;
     constexpr int STAGE = 2 * P * D * (int)sizeof(T);
     AttnParams p = p0;
-    const size_t fixed = attn_smem_bytes(0, STAGE, NW, GMAX, D, P, MMA, p.B);
+    // Pick the number of consumer warps (4..NW) that allows the deepest ring
+    // whose depth is a multiple of it (each stage owned by one consumer warp).
     const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int);
-    int stages = (int)((smem_budget - fixed) / per);
-    if (stages > 32) stages = 32;
+    int stages = 0, consumers = 0;
+    for (int nw = NW; nw >= 1; --nw) {
+        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B);
+        if (fixed >= smem_budget) continue;
+        int s = (int)((smem_budget - fixed) / per);
+        if (s > 32) s = 32;
+        const int c = s < nw ? s : nw;
+        if (c < 1) continue;
+        s = s / c * c;
+        if (s > stages || (s == stages && c > consumers)) { stages = s; consumers = c; }
+        if (nw <= 4 && stages >= 2) break;
+    }
     if (stages < 2) return cudaErrorInvalidConfiguration;
-    const int consumers = stages < NW ? stages : NW;
-    stages = stages / consumers * consumers;    // each stage owned by one consumer warp
     p.stages = stages;
     p.consumers = consumers;
-    const size_t smem = attn_smem_bytes(stages, STAGE, NW, GMAX, D, P, MMA, p.B);
+    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B);
     auto kern = attn_kernel<T, D, P, MMA, GMAX, NW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
