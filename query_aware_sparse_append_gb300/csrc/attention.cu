@@ -71,7 +71,6 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     constexpr int STAGE = 2 * TILE;
     constexpr int NSUB = D * ES / 128;          // 128-byte column boxes per tile
     constexpr int BOXW = 128 / ES;              // elements per box row
-    constexpr int NCT = NW * 32;                // consumer threads
     static_assert(TILE % 1024 == 0, "tile must keep 1024-byte swizzle alignment");
 
     extern __shared__ unsigned char smem_raw[];
@@ -90,8 +89,10 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     float *ff_p = ff_q + (MMA ? 0 : NWK * GMAX * D);               // FFMA only: [NWK][GMAX][P]
     int *prefix = reinterpret_cast<int *>(ff_p + (MMA ? 0 : NWK * GMAX * P));  // [B + 1]
     int *lens = prefix + (p.B + 1);                                // [B]
-    __shared__ int s_flag;       // last-arriver flag
     __shared__ int s_abort;      // a bounded wait gave up
+    // segment hand-off: [0] completes when the NWK working warps have written
+    // their states for a segment; [1] completes when the combiner has read them
+    __shared__ __align__(8) uint64_t seg_bar[2];
     volatile int *abort_flag = &s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -105,7 +106,11 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             mbar_init(&empty_bar[s], 1);
             last_ph[s] = -1;
         }
-        if (lane == 0) s_abort = 0;
+        if (lane == 0) {
+            s_abort = 0;
+            mbar_init(&seg_bar[0], (uint32_t)NWK);
+            mbar_init(&seg_bar[1], 1);
+        }
         fence_barrier_init();
         if (lane == 0) {
             prefetch_tensormap(&kmap);
@@ -293,11 +298,143 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         return;
     }
 
+    // A working warp may overwrite the shared state slot for segment k once the
+    // combiner has read segment k-1 (phase k-1 of the "free" barrier).
+    auto wait_slot_free = [&](uint32_t k) -> bool {
+        if (mbar_wait_bounded(&seg_bar[1], (k & 1u) ^ 1u, p.wait_limit_ns)) return true;
+        if (lane == 0) {
+            if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        return false;
+    };
+
+    // The combiner: for every segment of the CTA range, in order, merge the
+    // working warps' (m, l, o) into registers, release the slot, then write the
+    // output (whole unit) or this CTA's partial plus the unit's page ticket; the
+    // CTA that completes a unit's ticket merges all its partials.
+    auto combine_segments = [&]() {
+        constexpr int JPH = D / 32;                    // elements per lane per head
+        long long g = g0;
+        uint32_t kseg = 0;
+        while (g < g1) {
+            int b, h, j0, cnt;
+            long long us;
+            locate(g, b, h, j0, us, cnt);
+            const long long ue = us + cnt;
+            const long long s1 = min(g1, ue);
+            const int u = b * Hkv + h;
+            if (!mbar_wait_bounded(&seg_bar[0], kseg & 1u, p.wait_limit_ns)) {
+                if (lane == 0) {
+                    if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                return;
+            }
+            float acc[GMAX][JPH], Mh[GMAX], Lh[GMAX];
+#pragma unroll
+            for (int hh = 0; hh < GMAX; ++hh) {
+                Mh[hh] = -INFINITY;
+                Lh[hh] = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < JPH; ++jj) acc[hh][jj] = 0.f;
+                if (hh >= G) continue;
+                for (int x = 0; x < NWK; ++x) Mh[hh] = fmaxf(Mh[hh], scr_m[x * GMAX + hh]);
+                if (Mh[hh] == -INFINITY) continue;
+                for (int x = 0; x < NWK; ++x) {
+                    const float f = exp2f(scr_m[x * GMAX + hh] - Mh[hh]);
+                    Lh[hh] += scr_l[x * GMAX + hh] * f;
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj)
+                        acc[hh][jj] = fmaf(scr_o[(x * GMAX + hh) * D + jj * 32 + lane], f, acc[hh][jj]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused
+            ++kseg;
+
+            T *ob = static_cast<T *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+            if (g == us && s1 == ue) {                  // the whole unit is in this CTA
+#pragma unroll
+                for (int hh = 0; hh < GMAX; ++hh) {
+                    if (hh >= G) break;
+                    const float inv = Lh[hh] > 0.f ? 1.f / Lh[hh] : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<T>::from_f(acc[hh][jj] * inv);
+                }
+                g = s1;
+                continue;
+            }
+            // partial: publish it, then take the unit's ticket.  __syncwarp orders
+            // the lanes' stores before lane 0's device-scope fence, which releases
+            // them with the atomic.  The ticket counts pages, so CTAs with an empty
+            // range (grid larger than the kept-page count) cannot leave it short.
+            const size_t slot = (size_t)u + c;
+#pragma unroll
+            for (int hh = 0; hh < GMAX; ++hh) {
+                if (hh >= G) break;
+#pragma unroll
+                for (int jj = 0; jj < JPH; ++jj) p.part_o[(slot * G + hh) * D + jj * 32 + lane] = acc[hh][jj];
+                if (lane == 0) {
+                    p.part_ml[(slot * G + hh) * 2] = Mh[hh];
+                    p.part_ml[(slot * G + hh) * 2 + 1] = Lh[hh];
+                }
+            }
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence();
+                const int npg = (int)(s1 - g);
+                const int prev = atomicAdd(&p.counters[u], npg);
+                __threadfence();
+                last = (prev + npg == cnt);
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
+#pragma unroll
+                for (int hh = 0; hh < GMAX; ++hh) {
+                    if (hh >= G) break;
+                    float M = -INFINITY;
+                    for (int x = cf; x <= cl; ++x) {
+                        if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;   // empty range
+                        M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(u + x) * G + hh) * 2]));
+                    }
+                    float Ls = 0.f, a[JPH];
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) a[jj] = 0.f;
+                    if (M != -INFINITY) {
+                        for (int x = cf; x <= cl; ++x) {
+                            if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;
+                            const size_t sl = (size_t)(u + x) * G + hh;
+                            const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - M);
+                            Ls += __ldcg(&p.part_ml[sl * 2 + 1]) * f;
+#pragma unroll
+                            for (int jj = 0; jj < JPH; ++jj) a[jj] = fmaf(__ldcg(&p.part_o[sl * D + jj * 32 + lane]), f, a[jj]);
+                        }
+                    }
+                    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<T>::from_f(a[jj] * inv);
+                }
+                if (lane == 0) p.counters[u] = 0;
+            }
+            g = s1;
+        }
+    };
+
     // ---------------------------------------------------------------- consumers
+    // Warps 1..NWK take pages; the last warp is the combiner, which merges the
+    // working warps' states at every unit boundary (segment) of the CTA range
+    // while they move on; any other warp has nothing to do.
     const int w = warp - 1;
-    const int ct = tid - 32;
-    const bool working = w < NWK;
+    if (w == NW - 1) {
+        combine_segments();
+        return;
+    }
+    if (w >= NWK) return;
     long long g = g0;
+    uint32_t kseg = 0;
     while (g < g1) {
         int b, h, j0, cnt;
         long long us;
@@ -314,7 +451,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         // complete out of order, so a stage shared by several warps could be
         // observed "full" while an older fill into it is still in flight).
         const int first = (int)(g - g0);
-        const int lastx = working ? (int)(s1 - g0) : first;
+        const int lastx = (int)(s1 - g0);
         int i = first + ((w - first % NWK) % NWK + NWK) % NWK;
         int s = i % S;
         uint32_t ph = (uint32_t)((i / S) & 1);
@@ -408,17 +545,17 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty_bar[s]);
             }
-            // export this warp's state
+            // hand this warp's state to the combiner
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 l0 += __shfl_xor_sync(0xffffffffu, l0, off);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, off);
             }
+            if (!wait_slot_free(kseg)) break;
             const int h0 = 2 * cq, h1 = 2 * cq + 1;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 const int ch = mt * 16 + nq;
-                if (!working) break;
                 if (h0 < G) {
                     scr_o[(w * GMAX + h0) * D + ch] = o[mt][0];
                     scr_o[(w * GMAX + h0) * D + ch + 8] = o[mt][2];
@@ -428,7 +565,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     scr_o[(w * GMAX + h1) * D + ch + 8] = o[mt][3];
                 }
             }
-            if (nq == 0 && working) {
+            if (nq == 0) {
                 if (h0 < G) { scr_m[w * GMAX + h0] = m0; scr_l[w * GMAX + h0] = l0; }
                 if (h1 < G) { scr_m[w * GMAX + h1] = m1; scr_l[w * GMAX + h1] = l1; }
             }
@@ -439,10 +576,9 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             constexpr int CPT = D / LPT;             // channels per lane for q.k
             constexpr int KCH = CPT / EPC;           // 16-byte chunks per lane for q.k
             constexpr int DPL = D / 32;              // channels per lane for p.v
-            float *qs = ff_q + (working ? w : 0) * GMAX * D;
-            float *ps = ff_p + (working ? w : 0) * GMAX * P;
-            if (working)
-                for (int e = lane; e < G * D; e += 32) qs[e] = elem<T>::to_f(qb[e]);
+            float *qs = ff_q + w * GMAX * D;
+            float *ps = ff_p + w * GMAX * P;
+            for (int e = lane; e < G * D; e += 32) qs[e] = elem<T>::to_f(qb[e]);
             __syncwarp();
             float o[GMAX][DPL], m[GMAX], l[GMAX];
 #pragma unroll
@@ -519,83 +655,18 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty_bar[s]);
             }
+            if (!wait_slot_free(kseg)) break;
 #pragma unroll
             for (int gg = 0; gg < GMAX; ++gg) {
-                if (gg >= G || !working) break;
+                if (gg >= G) break;
 #pragma unroll
                 for (int x = 0; x < DPL; ++x) scr_o[(w * GMAX + gg) * D + lane * DPL + x] = o[gg][x];
                 if (lane == 0) { scr_m[w * GMAX + gg] = m[gg]; scr_l[w * GMAX + gg] = l[gg]; }
             }
         }
-
-        // --------------------------------------------- merge the consumer warps
-        named_barrier_sync(1, NCT);
-        const bool whole = (g == us) && (s1 == ue);
-        const int slot = u + c;
-        for (int e = ct; e < G * D; e += NCT) {
-            const int hh = e / D, ch = e - hh * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int x = 0; x < NWK; ++x) M = fmaxf(M, scr_m[x * GMAX + hh]);
-            float Ls = 0.f, acc = 0.f;
-            if (M != -INFINITY) {
-                for (int x = 0; x < NWK; ++x) {
-                    const float f = exp2f(scr_m[x * GMAX + hh] - M);
-                    Ls += scr_l[x * GMAX + hh] * f;
-                    acc += scr_o[(x * GMAX + hh) * D + ch] * f;
-                }
-            }
-            if (whole) {
-                static_cast<T *>(p.out)[((size_t)b * p.Hq + (size_t)h * G + hh) * D + ch] =
-                    elem<T>::from_f(Ls > 0.f ? acc / Ls : 0.f);
-            } else {
-                p.part_o[((size_t)slot * G + hh) * D + ch] = acc;
-                if (ch == 0) {
-                    p.part_ml[((size_t)slot * G + hh) * 2] = M;
-                    p.part_ml[((size_t)slot * G + hh) * 2 + 1] = Ls;
-                }
-            }
-        }
-        if (!whole) {
-            // publish the partial: the barrier orders every consumer's stores before
-            // thread 0's device-scope fence, which releases them with the ticket.
-            // The ticket counts pages, so CTAs whose range is empty (grid larger
-            // than the number of kept pages) cannot leave it short.
-            named_barrier_sync(1, NCT);
-            const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
-            if (ct == 0) {
-                __threadfence();
-                const int npg = (int)(s1 - g);
-                const int prev = atomicAdd(&p.counters[u], npg);
-                __threadfence();
-                s_flag = (prev + npg == cnt);
-            }
-            named_barrier_sync(1, NCT);
-            if (s_flag) {
-                for (int e = ct; e < G * D; e += NCT) {
-                    const int hh = e / D, ch = e - hh * D;
-                    float M = -INFINITY;
-                    for (int x = cf; x <= cl; ++x) {
-                        if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;   // empty range
-                        M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(u + x) * G + hh) * 2]));
-                    }
-                    float Ls = 0.f, acc = 0.f;
-                    if (M != -INFINITY) {
-                        for (int x = cf; x <= cl; ++x) {
-                            if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;
-                            const size_t sl = (size_t)(u + x) * G + hh;
-                            const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - M);
-                            Ls += __ldcg(&p.part_ml[sl * 2 + 1]) * f;
-                            acc += __ldcg(&p.part_o[sl * D + ch]) * f;
-                        }
-                    }
-                    static_cast<T *>(p.out)[((size_t)b * p.Hq + (size_t)h * G + hh) * D + ch] =
-                        elem<T>::from_f(Ls > 0.f ? acc / Ls : 0.f);
-                }
-                if (ct == 0) p.counters[u] = 0;
-            }
-        }
-        named_barrier_sync(1, NCT);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&seg_bar[0]);
+        ++kseg;
         g = s1;
     }
 }
@@ -608,11 +679,11 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     constexpr int NW = 8;
     constexpr int STAGE = 2 * P * D * (int)sizeof(T);
     AttnParams p = p0;
-    // Pick the number of consumer warps (4..NW) that allows the deepest ring
+    // Pick the number of working consumer warps (4..NW-1) that allows the deepest ring
     // whose depth is a multiple of it (each stage owned by one consumer warp).
     const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int);
     int stages = 0, consumers = 0;
-    for (int nw = NW; nw >= 1; --nw) {
+    for (int nw = NW - 1; nw >= 1; --nw) {   // the last consumer warp is the combiner
         const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);
