@@ -260,7 +260,12 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     aborted = true;
                     break;
                 }
-                if (pending && mbar_test_wait(&empty_bar[s_l], ph_l ^ 1u)) {
+                const bool ready = pending && mbar_test_wait(&empty_bar[s_l], ph_l ^ 1u);
+                if (!__any_sync(0xffffffffu, ready)) {   // nothing free yet: back off
+                    __nanosleep(64);
+                    continue;
+                }
+                if (ready) {
                     info[s_l].page = page;
                     info[s_l].nvalid = nvalid;
                     unsigned char *st = ring + (size_t)s_l * STAGE;
@@ -324,7 +329,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             const long long ue = us + cnt;
             const long long s1 = min(g1, ue);
             const int u = b * Hkv + h;
-            if (!mbar_wait_bounded(&seg_bar[0], kseg & 1u, p.wait_limit_ns)) {
+            if (!mbar_wait_sleepy(&seg_bar[0], kseg & 1u, p.wait_limit_ns, 256)) {
                 if (lane == 0) {
                     if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
                     *abort_flag = 1;
