@@ -62,6 +62,18 @@ __device__ __forceinline__ int cta_of(long long g, int C, long long T) {
     return (int)(((g + 1) * C - 1) / T);
 }
 
+// Online merge of one softmax state (m, l, o[]) into a running one (log2 domain).
+template <int J>
+__device__ __forceinline__ void merge_state(float &M, float &L, float *o, float m, float l, const float *ox) {
+    if (m == -INFINITY) return;
+    const float nm = fmaxf(M, m);
+    const float a = exp2f(M - nm), b = exp2f(m - nm);   // a = 0 while the running state is empty
+    L = L * a + l * b;
+#pragma unroll
+    for (int j = 0; j < J; ++j) o[j] = o[j] * a + ox[j] * b;
+    M = nm;
+}
+
 template <typename T, int D, int P, bool MMA, int GMAX, int NW>
 __global__ void __launch_bounds__(32 * (NW + 1), 1)
 attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -336,6 +348,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 }
                 return;
             }
+            // online merge over the working warps; one warp's loads are all
+            // independent, so they overlap instead of forming a chain
             float acc[GMAX][JPH], Mh[GMAX], Lh[GMAX];
 #pragma unroll
             for (int hh = 0; hh < GMAX; ++hh) {
@@ -343,16 +357,19 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 Lh[hh] = 0.f;
 #pragma unroll
                 for (int jj = 0; jj < JPH; ++jj) acc[hh][jj] = 0.f;
-                if (hh >= G) continue;
-                for (int x = 0; x < NWK; ++x) Mh[hh] = fmaxf(Mh[hh], scr_m[x * GMAX + hh]);
-                if (Mh[hh] == -INFINITY) continue;
-                for (int x = 0; x < NWK; ++x) {
-                    const float f = exp2f(scr_m[x * GMAX + hh] - Mh[hh]);
-                    Lh[hh] += scr_l[x * GMAX + hh] * f;
+            }
+            for (int x = 0; x < NWK; ++x) {
+                float mx[GMAX], lx[GMAX], ox[GMAX][JPH];
 #pragma unroll
-                    for (int jj = 0; jj < JPH; ++jj)
-                        acc[hh][jj] = fmaf(scr_o[(x * GMAX + hh) * D + jj * 32 + lane], f, acc[hh][jj]);
+                for (int hh = 0; hh < GMAX; ++hh) {
+                    const bool on = hh < G;
+                    mx[hh] = on ? scr_m[x * GMAX + hh] : -INFINITY;
+                    lx[hh] = on ? scr_l[x * GMAX + hh] : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) ox[hh][jj] = on ? scr_o[(x * GMAX + hh) * D + jj * 32 + lane] : 0.f;
                 }
+#pragma unroll
+                for (int hh = 0; hh < GMAX; ++hh) merge_state<JPH>(Mh[hh], Lh[hh], acc[hh], mx[hh], lx[hh], ox[hh]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused
@@ -399,28 +416,32 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
 #pragma unroll
                 for (int hh = 0; hh < GMAX; ++hh) {
+                    Mh[hh] = -INFINITY;
+                    Lh[hh] = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) acc[hh][jj] = 0.f;
+                }
+                for (int x = cf; x <= cl; ++x) {
+                    if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;   // empty range
+                    const size_t sb = (size_t)(u + x) * G;
+                    float mx[GMAX], lx[GMAX], ox[GMAX][JPH];
+#pragma unroll
+                    for (int hh = 0; hh < GMAX; ++hh) {
+                        const bool on = hh < G;
+                        mx[hh] = on ? __ldcg(&p.part_ml[(sb + hh) * 2]) : -INFINITY;
+                        lx[hh] = on ? __ldcg(&p.part_ml[(sb + hh) * 2 + 1]) : 0.f;
+#pragma unroll
+                        for (int jj = 0; jj < JPH; ++jj) ox[hh][jj] = on ? __ldcg(&p.part_o[(sb + hh) * D + jj * 32 + lane]) : 0.f;
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < GMAX; ++hh) merge_state<JPH>(Mh[hh], Lh[hh], acc[hh], mx[hh], lx[hh], ox[hh]);
+                }
+#pragma unroll
+                for (int hh = 0; hh < GMAX; ++hh) {
                     if (hh >= G) break;
-                    float M = -INFINITY;
-                    for (int x = cf; x <= cl; ++x) {
-                        if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;   // empty range
-                        M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(u + x) * G + hh) * 2]));
-                    }
-                    float Ls = 0.f, a[JPH];
+                    const float inv = Lh[hh] > 0.f ? 1.f / Lh[hh] : 0.f;
 #pragma unroll
-                    for (int jj = 0; jj < JPH; ++jj) a[jj] = 0.f;
-                    if (M != -INFINITY) {
-                        for (int x = cf; x <= cl; ++x) {
-                            if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;
-                            const size_t sl = (size_t)(u + x) * G + hh;
-                            const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - M);
-                            Ls += __ldcg(&p.part_ml[sl * 2 + 1]) * f;
-#pragma unroll
-                            for (int jj = 0; jj < JPH; ++jj) a[jj] = fmaf(__ldcg(&p.part_o[sl * D + jj * 32 + lane]), f, a[jj]);
-                        }
-                    }
-                    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<T>::from_f(a[jj] * inv);
+                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<T>::from_f(acc[hh][jj] * inv);
                 }
                 if (lane == 0) p.counters[u] = 0;
             }
