@@ -188,6 +188,36 @@ qasa_status qasa_dense_decode_attention(const qasa_kv_cache *cache, const void *
                                         size_t workspace_bytes, int32_t batch,
                                         int32_t *device_status, cudaStream_t stream);
 
+/* Bytes of the fixed device buffer that qasa_sparse_decode_attention_noalloc
+ * uses in place of a workspace (held by every device that loads the library). */
+#define QASA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * The decode step of qasa_sparse_decode_attention for callers that cannot
+ * allocate device memory: callers whose device memory belongs to a host
+ * framework that forbids allocating behind its back, and callers on paths
+ * where a device-synchronising call such as cudaMalloc is not allowed.  The
+ * paper has no counterpart; this is a deployment convenience.
+ *
+ * Arguments and results as in qasa_sparse_decode_attention, without the
+ * workspace: the library's own fixed buffer of QASA_NOALLOC_SCRATCH_BYTES
+ * serves instead, and nothing is allocated (no cudaMalloc, cudaFree or other
+ * allocating routine).  A shape whose qasa_decode_workspace_size exceeds that
+ * size is rejected with QASA_ERR_WORKSPACE before any launch.
+ *   - The first call on a device (that device current) looks up the buffer's
+ *     device address once; make that first call before any stream capture.
+ *   - All calls on a device share the buffer, which keeps the last call's
+ *     contents; what must start at zero is cleared inside each call.  Calls
+ *     that overlap on the GPU (other streams) race: serialise them.
+ */
+qasa_status qasa_sparse_decode_attention_noalloc(const qasa_kv_cache *cache, const void *q,
+                                                 int32_t num_q_heads, const int32_t *block_table,
+                                                 int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                                 const int32_t *budget_pages, int32_t max_budget,
+                                                 float scale, void *out, int32_t *selected,
+                                                 float *scores_out, int32_t batch,
+                                                 int32_t *device_status, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char *qasa_status_string(qasa_status status);
 

@@ -58,13 +58,17 @@ _lib.qasa_sparse_decode_attention.restype = _I
 _lib.qasa_dense_decode_attention.argtypes = [_C, _P, _I, _P, _I, _P, ctypes.c_float, _P, _P,
                                              ctypes.c_size_t, _I, _P, _P]
 _lib.qasa_dense_decode_attention.restype = _I
+_lib.qasa_sparse_decode_attention_noalloc.argtypes = [_C, _P, _I, _P, _I, _P, _P, _I, ctypes.c_float,
+                                                      _P, _P, _P, _I, _P, _P]
+_lib.qasa_sparse_decode_attention_noalloc.restype = _I
 _lib.qasa_status_string.argtypes = [_I]
 _lib.qasa_status_string.restype = ctypes.c_char_p
 _lib.qasa_version.restype = _I
 
 EXPORTED = ("qasa_kv_append", "qasa_decode_workspace_size", "qasa_select_pages",
             "qasa_sparse_attention", "qasa_sparse_decode_attention",
-            "qasa_dense_decode_attention", "qasa_status_string", "qasa_version")
+            "qasa_dense_decode_attention", "qasa_sparse_decode_attention_noalloc",
+            "qasa_status_string", "qasa_version")
 
 
 class QasaError(RuntimeError):
@@ -248,6 +252,24 @@ def sparse_decode_attention(cache: PagedKVCache, q: torch.Tensor, block_table: t
                                              workspace.numel(), B, _ptr(status), _stream(stream))
     _check(code, "qasa_sparse_decode_attention")
     return out, selected
+
+
+def sparse_decode_attention_noalloc(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                                    seq_lens: torch.Tensor, budget, max_budget: int,
+                                    out: torch.Tensor, selected: torch.Tensor,
+                                    scale: Optional[float] = None,
+                                    scores: Optional[torch.Tensor] = None,
+                                    status: Optional[torch.Tensor] = None, stream=None) -> int:
+    """The decode step without a workspace, for callers that cannot allocate
+    device memory: the library's fixed device buffer serves as scratch (see
+    qasa.h).  The caller passes every input and output; returns the status code
+    (QASA_ERR_WORKSPACE when the shape needs more scratch than the buffer)."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    bud = budget if isinstance(budget, torch.Tensor) else budget_pages(budget, seq_lens, cache.page_size)
+    return int(_lib.qasa_sparse_decode_attention_noalloc(
+        cache.c_ref, _ptr(_contig(q, "q")), Hq, _ptr(block_table), int(block_table.shape[1]),
+        _ptr(seq_lens), _ptr(bud), int(max_budget), float(scale or 0.0), _ptr(out), _ptr(selected),
+        _ptr(scores), B, _ptr(status), _stream(stream)))
 
 
 def dense_decode_attention(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
