@@ -197,6 +197,22 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         ustart = (long long)Hkv * prefix[b] + (long long)h * cnt;
     };
 
+    // The range is processed rotated: first [gL, g1), the part of the range's
+    // last unit that lies in it, then [g0, gL).  Both partial units of a range
+    // (its first and its last) are therefore done early, so every split unit's
+    // ticket completes mid-kernel and the range ends on whole units.
+    const long long n_loc = g1 - g0;
+    long long gL = g0;
+    if (n_loc > 0) {
+        int b, h, j, cnt;
+        long long us;
+        locate(g1 - 1, b, h, j, us, cnt);
+        if (us > g0) gL = us;
+    }
+    const long long nL = g1 - gL;
+    auto rot = [&](long long pos) -> long long { return pos < nL ? gL + pos : g0 + (pos - nL); };
+    auto run_end = [&](long long pos) -> long long { return pos < nL ? g1 : gL; };
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // Pages are handled in batches of WB <= min(32, S): the lanes resolve one
@@ -211,14 +227,14 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         // is issued, so their latency hides behind the ring instead of stalling it.
         struct Look { int page, phys, b, h; bool active, ok; };
         auto look_a = [&](long long bb, Look &lk) {      // locate; load the kept id
-            const long long gg = bb + lane;
-            lk.active = lane < WB && gg < g1;
+            const long long pos = bb + lane;
+            lk.active = lane < WB && pos < n_loc;
             lk.ok = false;
             lk.page = -1; lk.phys = -1; lk.b = 0; lk.h = 0;
             if (lk.active) {
                 int j, cnt;
                 long long us;
-                locate(gg, lk.b, lk.h, j, us, cnt);
+                locate(rot(pos), lk.b, lk.h, j, us, cnt);
                 lk.page = p.dense ? j : p.selected[((size_t)lk.b * Hkv + lk.h) * p.max_budget + j];
             }
         };
@@ -233,11 +249,11 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             lk.phys = p.block_table[(size_t)lk.b * p.max_pages + lk.page];
         };
         Look la, lb, lc;
-        look_a(g0, la);
+        look_a(0, la);
         look_b(la);
-        look_a(g0 + WB, lb);
-        for (long long base = g0; base < g1 && !aborted; base += WB) {
-            const int nb = (int)min((long long)WB, g1 - base);
+        look_a(WB, lb);
+        for (long long base = 0; base < n_loc && !aborted; base += WB) {
+            const int nb = (int)min((long long)WB, n_loc - base);
             int nvalid = 0, row = 0;
             const int page = la.page;
             if (la.active && la.ok) {                    // check the physical page
@@ -332,14 +348,16 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     // CTA that completes a unit's ticket merges all its partials.
     auto combine_segments = [&]() {
         constexpr int JPH = D / 32;                    // elements per lane per head
-        long long g = g0;
+        long long pos = 0;
         uint32_t kseg = 0;
-        while (g < g1) {
+        while (pos < n_loc) {
+            const long long g = rot(pos);
             int b, h, j0, cnt;
             long long us;
             locate(g, b, h, j0, us, cnt);
             const long long ue = us + cnt;
-            const long long s1 = min(g1, ue);
+            const long long s1 = min(run_end(pos), ue);
+            pos += s1 - g;
             const int u = b * Hkv + h;
             if (!mbar_wait_sleepy(&seg_bar[0], kseg & 1u, p.wait_limit_ns, 256)) {
                 if (lane == 0) {
@@ -384,12 +402,11 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
 #pragma unroll
                     for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<T>::from_f(acc[hh][jj] * inv);
                 }
-                g = s1;
                 continue;
             }
             // partial: publish it, then take the unit's ticket.  __syncwarp orders
-            // the lanes' stores before lane 0's device-scope fence, which releases
-            // them with the atomic.  The ticket counts pages, so CTAs with an empty
+            // the lanes' stores before lane 0's acquire-release atomic, which
+            // publishes them and makes the other CTAs' partials visible.  The ticket counts pages, so CTAs with an empty
             // range (grid larger than the kept-page count) cannot leave it short.
             const size_t slot = (size_t)u + c;
 #pragma unroll
@@ -405,13 +422,12 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             __syncwarp();
             int last = 0;
             if (lane == 0) {
-                __threadfence();
                 const int npg = (int)(s1 - g);
-                const int prev = atomicAdd(&p.counters[u], npg);
-                __threadfence();
+                const int prev = atomic_add_acq_rel_gpu(&p.counters[u], npg);   // release ours, acquire theirs
                 last = (prev + npg == cnt);
             }
             last = __shfl_sync(0xffffffffu, last, 0);
+            __syncwarp();
             if (last) {
                 const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
 #pragma unroll
@@ -445,7 +461,6 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 }
                 if (lane == 0) p.counters[u] = 0;
             }
-            g = s1;
         }
     };
 
@@ -459,15 +474,15 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         return;
     }
     if (w >= NWK) return;
-    long long g = g0;
+    long long pos = 0;
     uint32_t kseg = 0;
-    while (g < g1) {
+    while (pos < n_loc) {
+        const long long g = rot(pos);
         int b, h, j0, cnt;
         long long us;
         locate(g, b, h, j0, us, cnt);
         const long long ue = us + cnt;
-        const long long s1 = min(g1, ue);
-        const int u = b * Hkv + h;
+        const long long s1 = min(run_end(pos), ue);
         const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
 
         // Page i of the CTA range goes to consumer warp i % NWK and ring stage
@@ -476,8 +491,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         // stage can then never alias with a fill two phases behind (copies
         // complete out of order, so a stage shared by several warps could be
         // observed "full" while an older fill into it is still in flight).
-        const int first = (int)(g - g0);
-        const int lastx = (int)(s1 - g0);
+        const int first = (int)pos;
+        const int lastx = (int)(pos + (s1 - g));
         int i = first + ((w - first % NWK) % NWK + NWK) % NWK;
         int s = i % S;
         uint32_t ph = (uint32_t)((i / S) & 1);
@@ -693,7 +708,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) mbar_arrive(&seg_bar[0]);
         ++kseg;
-        g = s1;
+        pos = lastx;
     }
 }
 
