@@ -208,6 +208,37 @@ def test_decode_step_append_then_attend():
 
 # ------------------------------------------------------------------ edge cases
 
+@pytest.mark.parametrize("name", ["tinyllama", "gpt2_345m", "headline_8k"])
+def test_selection_with_exact_ties_and_mixed_signs(name):
+    # pages copied verbatim share their box, hence their score exactly: the tie
+    # must go to the lower page index; pages pushed against q score negative,
+    # so the keys of one unit span both signs (every radix bit in play)
+    from query_aware_sparse_append_gb300 import paged
+    cfg = W.CONFIGS[name]
+    case = H.make_case(cfg, seed=31, batch=3, device=False)
+    P, G = cfg.page_size, cfg.group
+    rng = np.random.default_rng(31)
+    for b, seq in enumerate(case.seqs):
+        k = W.widen(seq.k, cfg.dtype).astype(np.float32)
+        N = -(-int(case.lens[b]) // P)
+        q = W.widen(seq.q, cfg.dtype).reshape(cfg.num_kv_heads, G, cfg.head_dim).mean(axis=1)
+        qn = q / np.linalg.norm(q, axis=-1, keepdims=True)
+        src = rng.choice(np.arange(1, N - 1), size=min(6, N - 2), replace=False)
+        for s0 in src:                               # duplicate each source page twice
+            for dst in rng.choice(np.arange(1, N - 1), size=2, replace=False):
+                if dst * P + P <= k.shape[0] and s0 * P + P <= k.shape[0]:
+                    k[dst * P:(dst + 1) * P] = k[s0 * P:(s0 + 1) * P]
+        for neg in rng.choice(np.arange(1, N - 1), size=min(4, N - 2), replace=False):
+            lo, hi = neg * P, min((neg + 1) * P, k.shape[0])
+            k[lo:hi] = -4.0 * np.sqrt(cfg.head_dim) * qn[None] + 0.01 * k[lo:hi]
+        seq.k = W.to_storage(k, cfg.dtype)
+    paged.load(case, poison=True)
+    out, sel, scores, st = run_sparse(case)
+    assert st == 0
+    check_units(case, out, sel, scores, all_units(case))
+
+
+
 def test_edge_lengths_and_budgets():
     cfg = W.CONFIGS["tinyllama"].with_batch(8)
     lens = np.array([0, 1, 15, 16, 17, 33, 4096, 100], dtype=np.int32)
@@ -221,6 +252,18 @@ def test_edge_lengths_and_budgets():
     v = W.widen(case.seqs[1].v[0], "f16")
     for h in range(cfg.num_kv_heads):
         assert np.allclose(o[1, h * 8:(h + 1) * 8], v[h][None], atol=1e-3, rtol=0)
+
+
+def test_long_sequences_beyond_register_held_selection():
+    # more than 1026 pages per sequence: the selection keeps its keys in shared
+    # memory instead of registers
+    cfg = W.CONFIGS["tinyllama"].with_batch(2)
+    lens = np.array([20000, 16500], dtype=np.int32)
+    budgets = np.array([100, 300], dtype=np.int32)
+    case = H.make_case(cfg, seed=33, lens=lens, budgets=budgets)
+    out, sel, scores, st = run_sparse(case)
+    assert st == 0
+    check_units(case, out, sel, scores, all_units(case))
 
 
 def test_budget_above_max_budget_is_clamped_and_reported():
