@@ -55,6 +55,7 @@ def _load():
             lib.oracle_decode_unit.argtypes = [ctypes.c_int] * 4 + [
                 _D, _D, _D, _D, _D, ctypes.c_int, ctypes.c_double, _D, _I, _D]
             lib.oracle_decode_unit.restype = ctypes.c_int
+            lib.oracle_page_attention_mass.argtypes = [ctypes.c_int] * 4 + [_D, _D, ctypes.c_double, _D]
             _lib = lib
     return _lib
 
@@ -162,6 +163,35 @@ def decode_unit(q, K, V, lo, hi, L: int, P: int, k: int, scale: Optional[float] 
                                    _dp(hi), int(k), float(scale), _dp(scores), _ip(sel),
                                    _dp(out))
     return scores[:N].copy(), sel[:n].copy(), out
+
+
+def page_attention_mass(q, K, L: int, P: int, scale: Optional[float] = None) -> np.ndarray:
+    """Per-page share of the dense attention mass (mean over the G heads)."""
+    q, K = _f64(q), _f64(K)
+    if q.ndim == 1:
+        q = q[None]
+    G, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    N = num_pages(L, P)
+    mass = np.zeros(max(N, 1))
+    _load().oracle_page_attention_mass(G, d, int(L), int(P), _dp(q), _dp(K), float(scale), _dp(mass))
+    return mass[:N].copy()
+
+
+def page_hit_rate(mass, selected, k: int) -> Tuple[int, float, float]:
+    """Compare a selection with the page mass of one (sequence, KV head).
+
+    T = the k pages of largest mass, equal masses taken in page order (a stable
+    sort of the negated masses).  Returns (|first k selected ids ∩ T|, mass of
+    the selected pages, mass of T).
+    """
+    mass = _f64(mass)
+    top = np.argsort(-mass, kind="stable")[:k]
+    sel = np.asarray(selected, dtype=np.int64)[:k]
+    in_top = np.zeros(len(mass), dtype=bool)
+    in_top[top] = True
+    return int(in_top[sel].sum()), float(mass[sel].sum()), float(mass[top].sum())
 
 
 def run_units(fn, items, threads: int = 1):

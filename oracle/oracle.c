@@ -202,3 +202,31 @@ int oracle_decode_unit(int G, int d, int L, int P, const double *q, const double
     oracle_attention(G, d, L, P, q, K, V, n, sel, scale, out);
     return n;
 }
+
+/* Share of the attention mass that falls on each page: the dense softmax
+ * weights of each of the G query heads over all tokens below L, summed per
+ * page and averaged over the heads.  mass: [N], sums to 1 when L > 0.  Used to
+ * measure how well a page selection covers the true attention (the page hit
+ * rate that the TinyServe abstract names beside cache reuse). */
+void oracle_page_attention_mass(int G, int d, int L, int P, const double *q, const double *K,
+                                double scale, double *mass)
+{
+    int N = num_pages_of(L, P);
+    for (int p = 0; p < N; ++p) mass[p] = 0.0;
+    if (L <= 0) return;
+    double *z = (double *)malloc(sizeof(double) * (size_t)L);
+    for (int g = 0; g < G; ++g) {
+        const double *qg = q + (size_t)g * d;
+        double m = -INFINITY;
+        for (int t = 0; t < L; ++t) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += qg[c] * K[(size_t)t * d + c];
+            z[t] = acc * scale;
+            if (z[t] > m) m = z[t];
+        }
+        double denom = 0.0;
+        for (int t = 0; t < L; ++t) denom += exp(z[t] - m);
+        for (int t = 0; t < L; ++t) mass[t / P] += exp(z[t] - m) / denom / G;
+    }
+    free(z);
+}

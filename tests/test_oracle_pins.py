@@ -248,3 +248,86 @@ def test_empty_sequence_gives_zeros():
     s, sel, out = oracle.decode_unit(np.ones((2, 4)), np.zeros((0, 4)), np.zeros((0, 4)),
                                      np.zeros((0, 4)), np.zeros((0, 4)), 0, 16, 4)
     assert len(sel) == 0 and np.all(out == 0)
+
+
+# ------------------------------------------- page attention mass and hit rate
+# The TinyServe abstract names the page hit rate without a definition; the
+# oracle measures it against the dense softmax mass on each page.
+
+def test_page_mass_equals_dense_attention_over_page_indicator_values():
+    # with V[t] = one-hot of t's page, the dense attention output of head g is
+    # exactly head g's mass per page; the mass is the mean over the heads
+    r = rng(30)
+    G, P, L = 3, 16, 70
+    N = -(-L // P)
+    d = 8
+    q, K = r.standard_normal((G, d)), r.standard_normal((L, d))
+    V = np.zeros((L, d))
+    V[np.arange(L), np.arange(L) // P] = 1.0
+    want = oracle.dense_attention(q, K, V, L, P)[:, :N].mean(axis=0)
+    got = oracle.page_attention_mass(q, K, L, P)
+    assert got.shape == (N,)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-16)
+
+
+def test_page_mass_of_equal_keys_is_token_share_with_ragged_tail():
+    G, d, P, L = 2, 8, 16, 53
+    K = np.tile(np.linspace(-1, 1, d), (L, 1))
+    q = rng(31).standard_normal((G, d))
+    got = oracle.page_attention_mass(q, K, L, P)
+    assert got.tolist() == pytest.approx([16 / 53, 16 / 53, 16 / 53, 5 / 53], rel=1e-14)
+
+
+def test_page_mass_closed_form_for_one_raised_page():
+    # tokens of page 2 have logit a*scale, all others 0
+    d, P, L, a = 4, 16, 64, 3.0
+    q = np.array([[2.0, 0, 0, 0]])
+    K = np.zeros((L, d))
+    K[32:48, 0] = a / 2.0
+    e = math.exp(a / math.sqrt(d))
+    got = oracle.page_attention_mass(q, K, L, P)
+    den = 16 * e + 48
+    assert got.tolist() == pytest.approx([16 / den, 16 / den, 16 * e / den, 16 / den], rel=1e-14)
+
+
+def test_page_mass_averages_heads_not_logits():
+    # two heads that each put all their weight on a different page
+    d, P, L = 2, 16, 32
+    K = np.zeros((L, d)); K[:16, 0] = 1.0; K[16:, 1] = 1.0
+    q = np.array([[800.0, 0.0], [0.0, 800.0]])
+    got = oracle.page_attention_mass(q, K, L, P)
+    assert got.tolist() == pytest.approx([0.5, 0.5], abs=1e-15)
+
+
+def test_page_mass_of_empty_sequence():
+    assert oracle.page_attention_mass(np.ones((1, 4)), np.zeros((0, 4)), 0, 16).shape == (0,)
+
+
+def test_hit_rate_hand_example():
+    mass = [0.1, 0.4, 0.2, 0.3]
+    assert oracle.page_hit_rate(mass, [0, 3], 2) == (1, pytest.approx(0.4), pytest.approx(0.7))
+    assert oracle.page_hit_rate(mass, [1, 3], 2) == (2, pytest.approx(0.7), pytest.approx(0.7))
+    # equal masses: the lower page ids are the top ones
+    assert oracle.page_hit_rate([0.25] * 4, [2, 3], 2) == (0, 0.5, 0.5)
+    assert oracle.page_hit_rate([0.25] * 4, [0, 3], 2)[0] == 1
+
+
+def test_hit_rate_against_brute_force_subsets():
+    import itertools
+    r = rng(32)
+    for trial in range(40):
+        N = int(r.integers(2, 9))
+        mass = r.integers(0, 4, size=N).astype(float)   # many ties
+        mass /= max(mass.sum(), 1.0)
+        k = int(r.integers(1, N + 1))
+        sel = np.sort(r.choice(N, size=k, replace=False))
+        hits, cov, best = oracle.page_hit_rate(mass, sel, k)
+        subsets = list(itertools.combinations(range(N), k))
+        best_sum = max(sum(mass[list(s)]) for s in subsets)
+        assert best == pytest.approx(best_sum, abs=1e-15)
+        assert cov == pytest.approx(sum(mass[sel]), abs=1e-15)
+        # the top set: largest sum, and among those the lexicographically
+        # smallest list of (-mass, page) pairs
+        top = min((s for s in subsets if abs(sum(mass[list(s)]) - best_sum) < 1e-15),
+                  key=lambda s: sorted((-mass[i], i) for i in s))
+        assert hits == len(set(top) & set(sel.tolist()))
