@@ -84,6 +84,16 @@ def algorithmic_bytes(cfg, lens, budgets):
     return int(sel.sum()), int(att.sum()), int(dense.sum())
 
 
+def rebuild_bytes(cfg, lens):
+    """Algorithmic bytes of rebuilding every page box: the valid keys read once,
+    the boxes written once, the block-table entries read."""
+    import numpy as np
+    es = 4 if cfg.dtype == "f32" else 2
+    lens = np.asarray(lens, dtype=np.int64)
+    n = (lens + cfg.page_size - 1) // cfg.page_size
+    return int(cfg.num_kv_heads * cfg.head_dim * es * (lens.sum() + 2 * n.sum()) + 4 * n.sum())
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -94,11 +104,26 @@ def measured_peak():
 
 
 def kernel_source_digest():
+    """Digest of what the attention kernel is compiled from: attention.cu and the
+    device helpers with comments and blank lines dropped, plus the AttnParams
+    block of the launch header (other parameter blocks there do not reach it)."""
     import hashlib
+    import re
+    csrc = os.path.join(ROOT, "query_aware_sparse_append_gb300", "csrc")
+
+    def code(text):
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+        return "\n".join(ln for ln in lines if ln.strip())
+
     h = hashlib.sha256()
-    for name in ("attention.cu", "qasa_device.cuh", "qasa_launch.h"):
-        with open(os.path.join(ROOT, "query_aware_sparse_append_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    for name in ("attention.cu", "qasa_device.cuh"):
+        with open(os.path.join(csrc, name)) as f:
+            h.update(code(f.read()).encode())
+    with open(os.path.join(csrc, "qasa_launch.h")) as f:
+        text = f.read()
+    i = text.index("struct AttnParams")
+    h.update(code(text[i:text.index("};", i) + 2]).encode())
     return h.hexdigest()[:16]
 
 
@@ -339,6 +364,76 @@ def config_block(cfg):
 
 # ------------------------------------------------------------ GPU leg
 
+def kept_counts(lens, budgets, page_size, max_budget):
+    """Pages kept per sequence (the selection's rule: every page when the budget
+    reaches the page count, else max(budget, the forced sink and newest pages))."""
+    import numpy as np
+    n = (np.asarray(lens, dtype=np.int64) + page_size - 1) // page_size
+    b = np.asarray(budgets, dtype=np.int64)
+    k = np.where(b >= n, n, np.maximum(b, np.minimum(n, 2)))
+    return np.minimum(k, max_budget)
+
+
+def hit_rate_stats(qasa, wl, budget_dev, budgets, max_budget, sel, mass=None):
+    """Page hit rate of the GPU selection against the dense attention mass, both
+    computed by the library's kernels.  Returns the summary dict of the JSON line."""
+    import numpy as np
+    import torch
+    cfg = wl.cfg
+    qasa.sparse_decode_attention(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev, budget_dev,
+                                 max_budget=max_budget, selected=sel)
+    mass = qasa.page_attention_mass(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev, mass=mass)
+    hits, cov, best = qasa.page_hit_rate(wl.cache, mass, wl.lens_dev, budget_dev, sel)
+    torch.cuda.synchronize()
+    k = kept_counts(wl.lens, budgets, cfg.page_size, max_budget)
+    kk = np.repeat(k[:, None], cfg.num_kv_heads, axis=1).astype(np.float64)
+    h, c, b = (x.cpu().numpy().astype(np.float64) for x in (hits, cov, best))
+    live = kk > 0
+    n = (np.asarray(wl.lens, dtype=np.int64) + cfg.page_size - 1) // cfg.page_size
+    return {
+        "hit_rate": float(h[live].sum() / kk[live].sum()),
+        "covered_mass": float(c[live].mean()),
+        "best_mass": float(b[live].mean()),
+        "covered_over_best": float((c[live] / np.maximum(b[live], 1e-30)).mean()),
+        "kept_fraction": float(k.sum() / max(n.sum(), 1)),
+        "units": int(live.sum()),
+    }
+
+
+def run_hit_rate_table(args):
+    """One JSON line per (workload, budget): the page hit rate of the selection
+    against the dense attention mass, on the synthetic workloads."""
+    import numpy as np
+    import torch
+    from query_aware_sparse_append_gb300 import build
+    build.build()
+    from query_aware_sparse_append_gb300 import binding as qasa
+    from query_aware_sparse_append_gb300 import paged
+    from query_aware_sparse_append_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    names = [args.config] if args.config != "all" else list(W.CONFIGS)
+    for name in names:
+        cfg = W.CONFIGS[name]
+        if args.batch:
+            cfg = cfg.with_batch(args.batch)
+        wl = paged.load(paged.generate(cfg, seed=args.seed), device=dev)
+        n = W.num_pages(wl.lens, cfg.page_size).astype(np.int64)
+        sweeps = [("own", wl.budgets)] + [
+            ("%d permille" % pm, np.maximum((n * pm + 999) // 1000, 1).astype(np.int32))
+            for pm in (50, 125, 250, 500)]
+        for label, bud in sweeps:
+            mb = max(2, int(kept_counts(wl.lens, bud, cfg.page_size, 1 << 30).max()))
+            sel = torch.empty((cfg.batch, cfg.num_kv_heads, mb), dtype=torch.int32, device=dev)
+            bud_dev = torch.from_numpy(np.ascontiguousarray(bud, dtype=np.int32)).to(dev)
+            st = hit_rate_stats(qasa, wl, bud_dev, bud, mb, sel)
+            print(json.dumps({"workload": name, "budget": label, "planted_pages": bool(
+                cfg.planted_count or cfg.planted_permille), **st}), flush=True)
+        del wl
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -439,6 +534,19 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     dense_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in evd)
 
+    # ---- page hit rate of the selection against the dense attention mass
+    hit = hit_rate_stats(qasa, wl, wl.budget_dev, wl.budgets, max_budget, sel)
+
+    # ---- bulk rebuild of every page box from the pool (same boxes written back)
+    evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    for a, b_ in evr:
+        flush.zero_()
+        a.record(stream)
+        qasa.rebuild_page_bounds(wl.cache, wl.block_table, wl.lens_dev, status=status)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    rebuild_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in evr[1:])
+
     # ---- end to end through the public API with pinned host buffers
     q_h = wl.q_dev.cpu().pin_memory()
     lens_h = wl.lens_dev.cpu().pin_memory()
@@ -476,6 +584,7 @@ def run_ours(args):
     if rank != 0:
         return 0
     sel_b, att_b, dense_b = algorithmic_bytes(cfg, wl.lens, wl.budgets)
+    rebuild_b = rebuild_bytes(cfg, wl.lens)
     peak, peak_kind = measured_peak()
     att_gbs = att_b / (att_ms * 1e-3) / 1e9
     step_gbs = (sel_b + att_b) / (ms * 1e-3) / 1e9
@@ -503,6 +612,10 @@ def run_ours(args):
                   "achieved_gbs": dense_b / (dense_ms * 1e-3) / 1e9,
                   "frac": dense_b / (dense_ms * 1e-3) / 1e9 / peak,
                   "speedup_sparse_over_dense": dense_ms / ms},
+        "page_hit_rate": hit,
+        "metadata_rebuild": {"ms": rebuild_ms, "bytes": rebuild_b,
+                             "achieved_gbs": rebuild_b / (rebuild_ms * 1e-3) / 1e9,
+                             "frac": rebuild_b / (rebuild_ms * 1e-3) / 1e9 / peak},
         "cpu_baseline": cpu,
         "e2e": {"value": world * B / (e2e_mean * 1e-3), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean},
@@ -523,6 +636,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--hit-rate-table", action="store_true",
+                    help="print the page hit rate per workload (--config all) and budget, then exit")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline (0 to skip)")
     args = ap.parse_args(argv)
@@ -530,6 +645,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.hit_rate_table:
+        return run_hit_rate_table(args)
     return run_ours(args)
 
 

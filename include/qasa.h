@@ -120,6 +120,26 @@ qasa_status qasa_kv_append(const qasa_kv_cache *cache, const int32_t *block_tabl
                            cudaStream_t stream);
 
 /*
+ * Rebuild the page boxes of whole sequences from the keys already in k_pool:
+ * for every sequence b and logical page p < ceil(seq_lens[b] / page_size), the
+ * box of physical page block_table[b][p] becomes the per-channel min / max of
+ * the keys in its valid slots (slot < seq_lens[b] - p * page_size).  For
+ * caches whose keys were written by something other than qasa_kv_append (a
+ * prefill kernel storing K/V directly, a pool restored or migrated), or to
+ * re-derive the boxes after the fact.  Bit-identical to the boxes
+ * qasa_kv_append maintains for the same keys (min / max are exact).
+ *   seq_lens       [batch] int32, current lengths
+ *   device_status  int32 or NULL (QASA_DEVERR_PAGE_ID: page skipped,
+ *                  QASA_DEVERR_SEQ_LEN: length clamped)
+ * A physical page listed by several sequences (shared prefix) must have the
+ * same number of valid slots in each, else the last writer wins.  Reads every
+ * valid key once; only page_bounds is written.
+ */
+qasa_status qasa_rebuild_page_bounds(const qasa_kv_cache *cache, const int32_t *block_table,
+                                     int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch,
+                                     int32_t *device_status, cudaStream_t stream);
+
+/*
  * Bytes of device workspace the decode calls need for this shape on the
  * CURRENT device (split-K partials and per-(sequence, KV head) counters).
  * The workspace is scratch: its contents need no initialisation and are
@@ -217,6 +237,46 @@ qasa_status qasa_sparse_decode_attention_noalloc(const qasa_kv_cache *cache, con
                                                  float scale, void *out, int32_t *selected,
                                                  float *scores_out, int32_t batch,
                                                  int32_t *device_status, cudaStream_t stream);
+
+/*
+ * Page hit-rate instrumentation (the TinyServe abstract lists the page hit
+ * rate among its analyses and gives no definition; this library measures it
+ * against dense attention).  Neither call is on the decode path.
+ *
+ * qasa_page_attention_mass: for every (sequence, KV head), the share of the
+ * dense softmax(scale * q.k) weight of its G query heads (over ALL tokens
+ * below seq_len) that falls on each logical page, averaged over the G heads.
+ *   mass     [batch][num_kv_heads][max_pages_per_seq] float out; entries of a
+ *            sequence sum to 1 (to fp32 rounding); entries >= N_b are left
+ *            untouched; a page with an invalid block-table entry gets 0 and
+ *            sets QASA_DEVERR_PAGE_ID.  4-byte alignment suffices.
+ * Other arguments as in qasa_dense_decode_attention.  Reads every key twice.
+ */
+qasa_status qasa_page_attention_mass(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
+                                     const int32_t *block_table, int32_t max_pages_per_seq,
+                                     const int32_t *seq_lens, float scale, float *mass,
+                                     int32_t batch, int32_t *device_status, cudaStream_t stream);
+
+/*
+ * qasa_page_hit_rate: compare a selection with the page mass.  For every
+ * (sequence, KV head) with k_b kept pages (k_b as in qasa_select_pages) and
+ * T = the k_b pages of largest mass (equal masses: the lower page id first):
+ *   hits          [batch][num_kv_heads] int32 out: |first k_b selected ids ∩ T|
+ *                 (the hit rate is hits / k_b)
+ *   covered_mass  [batch][num_kv_heads] float out: mass summed over the
+ *                 selected pages
+ *   best_mass     [batch][num_kv_heads] float out: mass summed over T (the
+ *                 most any selection of k_b pages can cover)
+ * mass comes from qasa_page_attention_mass; selected ids are assumed distinct
+ * (as qasa_select_pages writes them); an id outside [0, N_b) is skipped and
+ * sets QASA_DEVERR_SELECTED.  Only the cache's shape fields are read.
+ * Device arrays need 4-byte alignment.
+ */
+qasa_status qasa_page_hit_rate(const qasa_kv_cache *cache, const float *mass, int32_t max_pages_per_seq,
+                               const int32_t *seq_lens, const int32_t *budget_pages,
+                               int32_t max_budget, const int32_t *selected, int32_t batch,
+                               int32_t *hits, float *covered_mass, float *best_mass,
+                               int32_t *device_status, cudaStream_t stream);
 
 /* Static description of a status code. */
 const char *qasa_status_string(qasa_status status);

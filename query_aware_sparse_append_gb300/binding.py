@@ -61,6 +61,12 @@ _lib.qasa_dense_decode_attention.restype = _I
 _lib.qasa_sparse_decode_attention_noalloc.argtypes = [_C, _P, _I, _P, _I, _P, _P, _I, ctypes.c_float,
                                                       _P, _P, _P, _I, _P, _P]
 _lib.qasa_sparse_decode_attention_noalloc.restype = _I
+_lib.qasa_rebuild_page_bounds.argtypes = [_C, _P, _I, _P, _I, _P, _P]
+_lib.qasa_rebuild_page_bounds.restype = _I
+_lib.qasa_page_attention_mass.argtypes = [_C, _P, _I, _P, _I, _P, ctypes.c_float, _P, _I, _P, _P]
+_lib.qasa_page_attention_mass.restype = _I
+_lib.qasa_page_hit_rate.argtypes = [_C, _P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P]
+_lib.qasa_page_hit_rate.restype = _I
 _lib.qasa_status_string.argtypes = [_I]
 _lib.qasa_status_string.restype = ctypes.c_char_p
 _lib.qasa_version.restype = _I
@@ -68,6 +74,7 @@ _lib.qasa_version.restype = _I
 EXPORTED = ("qasa_kv_append", "qasa_decode_workspace_size", "qasa_select_pages",
             "qasa_sparse_attention", "qasa_sparse_decode_attention",
             "qasa_dense_decode_attention", "qasa_sparse_decode_attention_noalloc",
+            "qasa_rebuild_page_bounds", "qasa_page_attention_mass", "qasa_page_hit_rate",
             "qasa_status_string", "qasa_version")
 
 
@@ -164,6 +171,16 @@ def kv_append(cache: PagedKVCache, block_table: torch.Tensor, seq_lens: torch.Te
                                _ptr(seq_lens), _ptr(append_lens), _ptr(k_new), _ptr(v_new), B, T,
                                _ptr(status), _stream(stream))
     _check(code, "qasa_kv_append")
+
+
+def rebuild_page_bounds(cache: PagedKVCache, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                        status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Recompute every page box of the batch from the keys in the pool."""
+    B = int(seq_lens.shape[0])
+    code = _lib.qasa_rebuild_page_bounds(cache.c_ref, _ptr(_contig(block_table, "block_table")),
+                                         int(block_table.shape[1]), _ptr(_contig(seq_lens, "seq_lens")), B,
+                                         _ptr(status), _stream(stream))
+    _check(code, "qasa_rebuild_page_bounds")
 
 
 def budget_pages(budget: Union[int, float, torch.Tensor], seq_lens: torch.Tensor,
@@ -289,6 +306,42 @@ def dense_decode_attention(cache: PagedKVCache, q: torch.Tensor, block_table: to
                                             workspace.numel(), B, _ptr(status), _stream(stream))
     _check(code, "qasa_dense_decode_attention")
     return out
+
+
+def page_attention_mass(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, scale: Optional[float] = None,
+                        mass: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Share of the dense attention of each (sequence, KV head) on each page,
+    [batch, num_kv_heads, max_pages_per_seq] float32 (pages >= N_b: zero when
+    ``mass`` is allocated here, untouched otherwise)."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    maxp = int(block_table.shape[1])
+    if mass is None:
+        mass = torch.zeros((B, cache.num_kv_heads, maxp), dtype=torch.float32, device=q.device)
+    code = _lib.qasa_page_attention_mass(cache.c_ref, _ptr(_contig(q, "q")), Hq, _ptr(block_table), maxp,
+                                         _ptr(seq_lens), float(scale or 0.0), _ptr(_contig(mass, "mass")),
+                                         B, _ptr(status), _stream(stream))
+    _check(code, "qasa_page_attention_mass")
+    return mass
+
+
+def page_hit_rate(cache: PagedKVCache, mass: torch.Tensor, seq_lens: torch.Tensor,
+                  budget_pages: torch.Tensor, selected: torch.Tensor,
+                  status: Optional[torch.Tensor] = None, stream=None):
+    """(hits int32, covered float32, best float32), each [batch, num_kv_heads]:
+    how many selected pages are among the k_b pages of largest mass, the mass
+    the selection covers and the largest mass any k_b pages cover."""
+    B, Hkv, maxp = (int(x) for x in mass.shape)
+    mb = int(selected.shape[2])
+    hits = torch.empty((B, Hkv), dtype=torch.int32, device=mass.device)
+    covered = torch.empty((B, Hkv), dtype=torch.float32, device=mass.device)
+    best = torch.empty((B, Hkv), dtype=torch.float32, device=mass.device)
+    code = _lib.qasa_page_hit_rate(cache.c_ref, _ptr(_contig(mass, "mass")), maxp, _ptr(seq_lens),
+                                   _ptr(budget_pages), mb, _ptr(_contig(selected, "selected")), B,
+                                   _ptr(hits), _ptr(covered), _ptr(best), _ptr(status), _stream(stream))
+    _check(code, "qasa_page_hit_rate")
+    return hits, covered, best
 
 
 def decode_device_errors(code: int) -> Sequence[str]:

@@ -267,6 +267,30 @@ qasa_status qasa_kv_append(const qasa_kv_cache *cache, const int32_t *block_tabl
     return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
 }
 
+qasa_status qasa_rebuild_page_bounds(const qasa_kv_cache *cache, const int32_t *block_table,
+                                     int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch,
+                                     int32_t *device_status, cudaStream_t stream) {
+    qasa_status st = check_cache(cache);
+    if (st != QASA_OK || batch == 0) return st;
+    if (!block_table || !seq_lens) return QASA_ERR_NULL;
+    if (batch < 0 || batch > kMaxBatch || max_pages_per_seq < 1 || max_pages_per_seq > kMaxPagesPerSeq)
+        return QASA_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return QASA_ERR_ALIGN;
+    RebuildParams p;
+    p.k_pool = cache->k_pool;
+    p.bounds = cache->page_bounds;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.status = device_status;
+    p.num_phys = cache->num_phys_pages;
+    p.Hkv = cache->num_kv_heads;
+    p.P = cache->page_size;
+    p.max_pages = max_pages_per_seq;
+    cudaError_t e = launch_rebuild_bounds(cache->dtype, cache->head_dim, p, batch, stream);
+    return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
+}
+
 size_t qasa_decode_workspace_size(int32_t batch, int32_t num_q_heads, const qasa_kv_cache *cache,
                                   int32_t max_pages_per_seq) {
     (void)max_pages_per_seq;
@@ -366,6 +390,67 @@ qasa_status qasa_dense_decode_attention(const qasa_kv_cache *cache, const void *
     return run_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, seq_lens,
                          2, nullptr, scale, out, workspace, workspace_bytes, batch, device_status,
                          true, false, stream);
+}
+
+qasa_status qasa_page_attention_mass(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
+                                     const int32_t *block_table, int32_t max_pages_per_seq,
+                                     const int32_t *seq_lens, float scale, float *mass,
+                                     int32_t batch, int32_t *device_status, cudaStream_t stream) {
+    if (batch == 0) return check_cache(cache);
+    qasa_status st = check_decode(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                                  q, batch);
+    if (st != QASA_OK) return st;
+    if (!mass) return QASA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(mass) & 3u) return QASA_ERR_ALIGN;
+    MassParams p;
+    p.k_pool = cache->k_pool;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.q = q;
+    p.mass = mass;
+    p.status = device_status;
+    p.num_phys = cache->num_phys_pages;
+    p.Hkv = cache->num_kv_heads;
+    p.P = cache->page_size;
+    p.G = num_q_heads / cache->num_kv_heads;
+    p.Hq = num_q_heads;
+    p.max_pages = max_pages_per_seq;
+    const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)cache->head_dim);
+    p.scale_log2 = (float)(sc * 1.4426950408889634);
+    cudaError_t e = launch_page_mass(cache->dtype, cache->head_dim, p, batch * cache->num_kv_heads, stream);
+    return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
+}
+
+qasa_status qasa_page_hit_rate(const qasa_kv_cache *cache, const float *mass, int32_t max_pages_per_seq,
+                               const int32_t *seq_lens, const int32_t *budget_pages,
+                               int32_t max_budget, const int32_t *selected, int32_t batch,
+                               int32_t *hits, float *covered_mass, float *best_mass,
+                               int32_t *device_status, cudaStream_t stream) {
+    qasa_status st = check_cache(cache);
+    if (st != QASA_OK || batch == 0) return st;
+    if (!mass || !seq_lens || !budget_pages || !selected || !hits || !covered_mass || !best_mass)
+        return QASA_ERR_NULL;
+    if (batch < 0 || batch > kMaxBatch) return QASA_ERR_SHAPE;
+    if (max_pages_per_seq < 1 || max_pages_per_seq > kMaxPagesPerSeq) return QASA_ERR_SHAPE;
+    if (max_budget < 2) return QASA_ERR_BUDGET;
+    const void *ptrs[] = {mass, seq_lens, budget_pages, selected, hits, covered_mass, best_mass};
+    for (const void *ptr : ptrs)
+        if (reinterpret_cast<uintptr_t>(ptr) & 3u) return QASA_ERR_ALIGN;
+    HitParams p;
+    p.mass = mass;
+    p.seq_lens = seq_lens;
+    p.budget = budget_pages;
+    p.selected = selected;
+    p.hits = hits;
+    p.covered = covered_mass;
+    p.best = best_mass;
+    p.status = device_status;
+    p.Hkv = cache->num_kv_heads;
+    p.P = cache->page_size;
+    p.max_pages = max_pages_per_seq;
+    p.max_budget = max_budget;
+    cudaError_t e = launch_page_hit(p, batch * cache->num_kv_heads, stream);
+    return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
 }
 
 const char *qasa_status_string(qasa_status s) {

@@ -14,15 +14,21 @@
 // takes the contiguous range [c*T/C, (c+1)*T/C).  A range covers whole units
 // (written straight to `out`) and at most two partial units at its ends,
 // whose partial (m, l, o) go to workspace slot (unit + c); the CTA that
-// finishes a unit last (atomic ticket counting the unit's pages, no waiting)
-// merges its partials.
+// finishes a unit last (acquire-release ticket counting the unit's pages, no
+// waiting) merges its partials.  Each CTA walks its range rotated (the part of
+// its last unit first), so both of its partial units finish early.
 //
-// Inside a CTA: warp 0 is the producer.  It turns kept page ids into physical
-// tiles through the block table and issues one tiled TMA box per 128 bytes of
-// head dimension for K and for V (cp.async.bulk.tensor, 128-byte swizzle) into
-// a ring of shared-memory stages guarded by mbarriers.  The other NW warps
-// consume pages round-robin.  For 16-bit KV and G >= 2 a consumer computes
-// S^T = K q^T and O^T += V^T P^T as m16n8k16 tensor-core MMAs (16 tokens x 8
+// Inside a CTA: warp 0 is the producer.  Its lanes turn up to 32 kept page ids
+// into physical tiles through the block table at once and each lane issues its
+// page's K and V copies: one 3-D tiled TMA box per tile (cp.async.bulk.tensor,
+// 128-byte swizzle; a 2-D box per 128 bytes of head dimension where the 3-D
+// map is refused) into a ring of shared-memory stages guarded by mbarriers.
+// NWK working warps consume the pages (page i of the range goes to warp
+// i % NWK and stage i % S, S a multiple of NWK, so a stage is only ever used by
+// one warp); the last warp merges the working warps' softmax states at every
+// unit boundary and writes the output or the partial.  For 16-bit KV and
+// G >= 2 a consumer computes S^T = K q^T and O^T += V^T P^T as m16n8k16
+// tensor-core MMAs (16 tokens x 8
 // query heads per MMA; ldmatrix reads the swizzled tiles conflict-free;
 // movmatrix turns the S accumulators into the P operand) with an online
 // softmax in fp32.  Otherwise (fp32 KV, or one query head per KV head, where

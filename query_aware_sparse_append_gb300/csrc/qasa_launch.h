@@ -56,10 +56,47 @@ struct AttnParams {
     unsigned long long wait_limit_ns;
 };
 
+struct MassParams {
+    const void *k_pool;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const void *q;
+    float *mass;       // [B][Hkv][max_pages]
+    int32_t *status;
+    int num_phys, Hkv, P, G, Hq, max_pages;
+    float scale_log2;
+};
+
+struct HitParams {
+    const float *mass;        // [B][Hkv][max_pages]
+    const int32_t *seq_lens;
+    const int32_t *budget;
+    const int32_t *selected;  // [B][Hkv][max_budget]
+    int32_t *hits;            // [B][Hkv]
+    float *covered;           // [B][Hkv]
+    float *best;              // [B][Hkv]
+    int32_t *status;
+    int Hkv, P, max_pages, max_budget;
+};
+
+struct RebuildParams {
+    const void *k_pool;
+    void *bounds;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    int32_t *status;
+    int num_phys, Hkv, P, max_pages;
+};
+
 cudaError_t launch_append(qasa_dtype dt, int D, const AppendParams &p, int batch, cudaStream_t stream);
 cudaError_t launch_select(qasa_dtype dt, int D, const SelectParams &p, int units, cudaStream_t stream);
 cudaError_t launch_attention(qasa_dtype dt, int D, int P, const CUtensorMap &km, const CUtensorMap &vm,
                              const AttnParams &p, int grid, size_t smem_budget, bool pdl,
                              cudaStream_t stream);
+
+cudaError_t launch_rebuild_bounds(qasa_dtype dt, int D, const RebuildParams &p, int batch,
+                                  cudaStream_t stream);
+cudaError_t launch_page_mass(qasa_dtype dt, int D, const MassParams &p, int units, cudaStream_t stream);
+cudaError_t launch_page_hit(const HitParams &p, int units, cudaStream_t stream);
 
 }  // namespace qasa
