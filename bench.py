@@ -521,6 +521,24 @@ def run_ours(args):
     sel_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev3)
     att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev3)
 
+    # ---- the same step in the other form (one cooperative launch <-> two launches)
+    single = os.environ.get("QASA_SINGLE_LAUNCH", "0") == "1"
+    os.environ["QASA_SINGLE_LAUNCH"] = "0" if single else "1"
+    try:
+        for _ in range(3):
+            step()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b_ in ev2:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+    finally:
+        os.environ["QASA_SINGLE_LAUNCH"] = "1" if single else "0"
+    other_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in ev2)
+
     # ---- dense path (every page), for comparison
     dense_out = torch.empty_like(out)
     evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -608,6 +626,10 @@ def run_ours(args):
                      "algorithmic_bytes": sel_b + att_b},
         "kernels_ms": {"select_pages": sel_ms, "sparse_attention": att_ms,
                        "select_gbs": sel_b / (sel_ms * 1e-3) / 1e9},
+        "step_form": "one cooperative launch (score + select + attend)" if single
+                     else "two launches (select, then attention)",
+        ("two_launch_step" if single else "single_launch_step"):
+            {"ms_per_step": other_ms, "queries_per_s": B / (other_ms * 1e-3)},
         "dense": {"ms_per_step": dense_ms, "queries_per_s": B / (dense_ms * 1e-3),
                   "achieved_gbs": dense_b / (dense_ms * 1e-3) / 1e9,
                   "frac": dense_b / (dense_ms * 1e-3) / 1e9 / peak,
@@ -619,7 +641,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": world * B / (e2e_mean * 1e-3), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if single else 2) * args.steps,
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)

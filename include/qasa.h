@@ -184,9 +184,24 @@ qasa_status qasa_sparse_attention(const qasa_kv_cache *cache, const void *q, int
                                   int32_t batch, int32_t *device_status, cudaStream_t stream);
 
 /*
- * One decode step: qasa_select_pages followed by qasa_sparse_attention on the
- * same stream (the second kernel's prologue overlaps the first's tail through
- * programmatic dependent launch).  Arguments as in those two calls.
+ * One decode step: the scoring and selection of qasa_select_pages and the
+ * attention of qasa_sparse_attention, with the same results.  Arguments as in
+ * those two calls.
+ *
+ * By default it runs as two kernels on the stream: selection, then attention
+ * (the attention kernel's prologue overlaps the selection's tail through
+ * programmatic dependent launch).  With QASA_SINGLE_LAUNCH=1 in the
+ * environment it runs as ONE cooperative launch of a persistent kernel (one
+ * CTA per SM) that scores, selects and attends (the single pass of the
+ * TinyServe abstract): each CTA selects the (sequence, KV head) units whose
+ * first kept page falls in its share of the kept pages and publishes each
+ * unit's ids with a flag, which the CTA's copy engine acquires (bounded wait)
+ * before reading them; the kept count of every unit follows from seq_lens and
+ * budget_pages alone, so the split of the attention work is known before any
+ * score; an 8-byte-per-unit region of the workspace is zeroed on the stream
+ * first.  If the cooperative launch is refused, the two kernels run instead.
+ * Selected ids and scores are identical in both forms; outputs agree to fp32
+ * summation order.
  */
 qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void *q,
                                          int32_t num_q_heads, const int32_t *block_table,

@@ -68,8 +68,24 @@ size_t smem_optin() {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace carve-up: counters [units] | partial (m, l) [(units + C) * G * 2] |
-// partial o [(units + C) * G * D], each region 256-byte aligned.
+// Internal status: the cooperative launch of the single-launch kernel was
+// refused (not every CTA can be resident); the caller falls back to two.
+constexpr qasa_status QASA_ERR_COOPERATIVE = static_cast<qasa_status>(100);
+
+// The decode step runs as two kernels (selection, then attention) unless
+// QASA_SINGLE_LAUNCH=1 asks for the single cooperative launch.  On GB300 the
+// two-kernel form is faster for every measured workload: inside one launch
+// only four warps per SM select, and a unit's selection (block-table row, box
+// scoring, radix select; ~20 us per unit, latency-bound) then paces the
+// attention streaming.
+bool single_launch_enabled() {
+    const char *v = std::getenv("QASA_SINGLE_LAUNCH");
+    return v && v[0] == '1';
+}
+
+// Workspace carve-up: counters [units], ready flags [units] | partial (m, l)
+// [(units + C) * G * 2] | partial o [(units + C) * G * D], each region
+// 256-byte aligned.
 struct WsLayout {
     size_t counters, part_ml, part_o, total;
 };
@@ -80,7 +96,7 @@ WsLayout ws_layout(int batch, int num_q_heads, const qasa_kv_cache *c, int grid)
     const size_t slots = units + (size_t)grid;
     WsLayout w;
     w.counters = 0;
-    w.part_ml = align_up(units * 4, 256);
+    w.part_ml = align_up(units * 8, 256);
     w.part_o = w.part_ml + align_up(slots * G * 2 * 4, 256);
     w.total = w.part_o + align_up(slots * G * (size_t)c->head_dim * 4, 256);
     return w;
@@ -164,11 +180,15 @@ qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_head
     return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
 }
 
+// Attention over kept pages (or every page when `dense`).  With `fused` the
+// same persistent kernel also scores and selects (one launch for the step);
+// it then writes `selected` and `scores_out`.
 qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_heads,
                           const int32_t *block_table, int max_pages, const int32_t *seq_lens,
                           const int32_t *budget_pages, int max_budget, const int32_t *selected,
                           float scale, void *out, void *workspace, size_t ws_bytes, int batch,
-                          int32_t *status, bool dense, bool pdl, cudaStream_t stream) {
+                          int32_t *status, bool dense, bool pdl, cudaStream_t stream,
+                          bool fused = false, float *scores_out = nullptr) {
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
     const WsLayout w = ws_layout(batch, num_q_heads, cache, grid);
@@ -194,13 +214,15 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
         }
     }
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    if (dense && cudaMemsetAsync(ws + w.counters, 0, (size_t)batch * cache->num_kv_heads * 4, stream) != cudaSuccess)
+    const size_t units = (size_t)batch * cache->num_kv_heads;
+    // tickets (and, for one launch, the ready flags) must start at zero
+    if ((dense || fused) && cudaMemsetAsync(ws + w.counters, 0, units * (fused ? 8 : 4), stream) != cudaSuccess)
         return QASA_ERR_CUDA;
     AttnParams p;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
     p.budget = budget_pages;
-    p.selected = selected;
+    p.selected = const_cast<int32_t *>(selected);   // written only by the single-launch kernel
     p.q = q;
     p.out = out;
     p.part_o = reinterpret_cast<float *>(ws + w.part_o);
@@ -221,12 +243,21 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     p.stages = 0;
     p.consumers = 0;
     p.wait_limit_ns = kWaitLimitNs;
+    p.bounds = cache->page_bounds;
+    p.scores_out = scores_out;
+    p.ready = reinterpret_cast<int32_t *>(ws + w.counters) + units;
     size_t budget = smem_optin();
     if (budget == 0) return QASA_ERR_CUDA;
     budget = budget > 1024 ? budget - 1024 : budget;   // leave room for static shared memory
-    cudaError_t e = launch_attention(cache->dtype, cache->head_dim, cache->page_size, km, vm, p, grid,
-                                     budget, pdl, stream);
+    cudaError_t e = fused ? launch_fused_decode(cache->dtype, cache->head_dim, cache->page_size, km, vm, p,
+                                                grid, budget, stream)
+                          : launch_attention(cache->dtype, cache->head_dim, cache->page_size, km, vm, p, grid,
+                                             budget, pdl, stream);
     if (e == cudaErrorInvalidConfiguration) return QASA_ERR_SHAPE;
+    if (e == cudaErrorCooperativeLaunchTooLarge) {   // not every CTA could be resident: two launches
+        (void)cudaGetLastError();
+        return QASA_ERR_COOPERATIVE;
+    }
     return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
 }
 
@@ -367,6 +398,12 @@ qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void 
         !aligned16(workspace))
         return QASA_ERR_WORKSPACE;
     if (batch == 0) return QASA_OK;
+    if (single_launch_enabled()) {
+        st = run_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
+                           max_budget, selected, scale, out, workspace, workspace_bytes, batch,
+                           device_status, false, false, stream, true, scores_out);
+        if (st != QASA_ERR_COOPERATIVE) return st;
+    }
     st = run_select(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
                     max_budget, selected, scores_out, static_cast<int32_t *>(workspace), batch,
                     device_status, stream);

@@ -36,8 +36,7 @@
 //
 // Every wait is bounded: a wait that gives up sets QASA_DEVERR_TIMEOUT, the CTA
 // stops issuing, drains the copies it issued (again bounded) and returns.
-#include "qasa_device.cuh"
-#include "qasa_launch.h"
+#include "select_device.cuh"
 
 namespace qasa {
 
@@ -47,8 +46,14 @@ struct StageInfo {
     int nvalid;  // valid tokens in the page (0: nothing to attend)
 };
 
+constexpr int kSelThreads = 128;   // selector warps of the single-launch kernel
+constexpr int kSelBarrier = 1;     // their named barrier
+constexpr int kSelSlotsPerWarp = 2;                    // box tiles in flight per selector warp
+constexpr int kSelStageSlots = 4 * kSelSlotsPerWarp;
+
 // Host-side size of the dynamic shared memory (mirrors the device carve-up).
-size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int P, bool mma, int B) {
+size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int P, bool mma, int B,
+                       bool fused, int max_pages) {
     size_t s = 1024;                                   // alignment slack for the ring
     s += (size_t)stages * stage_bytes;
     s += (size_t)stages * 2 * sizeof(uint64_t);        // full / empty barriers
@@ -56,6 +61,12 @@ size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int
     s += (size_t)nw * gmax * (D + 2) * sizeof(float);  // combine scratch
     if (!mma) s += (size_t)nw * gmax * (D + P) * sizeof(float);
     s += (size_t)(2 * B + 2) * sizeof(int);            // prefix, lengths
+    if (fused) {
+        // selector scratch: scores, block-table row, box staging slots + barriers
+        s += 16 + (size_t)max_pages * sizeof(float) + sizeof(SelScratch);
+        s += 16 + (size_t)max_pages * sizeof(int32_t);
+        if (mma) s += 16 + (size_t)kSelStageSlots * (16 * (2 * D * 2 + 64) + sizeof(uint64_t));
+    }
     s += 64;
     return s;
 }
@@ -80,8 +91,8 @@ __device__ __forceinline__ void merge_state(float &M, float &L, float *o, float 
     M = nm;
 }
 
-template <typename T, int D, int P, bool MMA, int GMAX, int NW>
-__global__ void __launch_bounds__(32 * (NW + 1), 1)
+template <typename T, int D, int P, bool MMA, int GMAX, int NW, bool FUSED>
+__global__ void __launch_bounds__(32 * (NW + 1) + (FUSED ? kSelThreads : 0), 1)
 attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
             AttnParams p) {
     constexpr int ES = (int)sizeof(T);
@@ -107,6 +118,16 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     float *ff_p = ff_q + (MMA ? 0 : NWK * GMAX * D);               // FFMA only: [NWK][GMAX][P]
     int *prefix = reinterpret_cast<int *>(ff_p + (MMA ? 0 : NWK * GMAX * P));  // [B + 1]
     int *lens = prefix + (p.B + 1);                                // [B]
+    // single launch: the selector warps' scores [max_pages], scratch, the
+    // unit's block-table row [max_pages] and (tensor-core scoring) the box
+    // staging slots with their barriers
+    float *sel_sc = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(lens + p.B) + 15) & ~uintptr_t(15));
+    SelScratch *sel_x = reinterpret_cast<SelScratch *>(sel_sc + (FUSED ? p.max_pages : 0));
+    int32_t *sel_phys = reinterpret_cast<int32_t *>((reinterpret_cast<uintptr_t>(sel_x + 1) + 15) & ~uintptr_t(15));
+    unsigned char *sel_buf = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(sel_phys + (FUSED ? p.max_pages : 0)) + 15) & ~uintptr_t(15));
+    constexpr int kSelTileB = 16 * (2 * D * ES + 64);
+    uint64_t *sel_bar = reinterpret_cast<uint64_t *>(sel_buf + (FUSED && MMA ? kSelStageSlots * kSelTileB : 0));
     __shared__ int s_abort;      // a bounded wait gave up
     // segment hand-off: [0] completes when the NWK working warps have written
     // their states for a segment; [1] completes when the combiner has read them
@@ -129,6 +150,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             mbar_init(&seg_bar[0], (uint32_t)NWK);
             mbar_init(&seg_bar[1], 1);
         }
+        if constexpr (FUSED && MMA)
+            for (int i = lane; i < kSelStageSlots; i += 32) mbar_init(&sel_bar[i], 1);
         fence_barrier_init();
         if (lane == 0) {
             prefetch_tensormap(&kmap);
@@ -182,6 +205,10 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 if ((b * Hkv + h) % C != c) continue;
                 T *o = static_cast<T *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
                 for (int i = tid; i < G * D; i += blockDim.x) o[i] = elem<T>::from_f(0.f);
+                if constexpr (FUSED) {   // and no kept ids
+                    int32_t *row = p.selected + ((size_t)b * Hkv + h) * p.max_budget;
+                    for (int i = tid; i < p.max_budget; i += blockDim.x) row[i] = -1;
+                }
             }
         }
     }
@@ -219,6 +246,65 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     auto rot = [&](long long pos) -> long long { return pos < nL ? gL + pos : g0 + (pos - nL); };
     auto run_end = [&](long long pos) -> long long { return pos < nL ? g1 : gL; };
 
+    if constexpr (FUSED) {
+        // -------------------------------------------------------- selectors
+        // The selector warps score and select the units whose first kept page
+        // lies in this CTA's range ("owned" units), in the order the range is
+        // consumed: the range's last unit first (the rotation starts there; a
+        // neighbour's range may start with it too), then the others ascending.
+        // Each unit's kept ids are published with a device-scope release of
+        // its ready flag, which the producers (here and in the neighbouring
+        // CTA) acquire before reading them.
+        if (warp > NW) {
+            const SelGroup<kSelThreads, kSelBarrier> grp{tid - 32 * (NW + 1)};
+            SelectParams sp;
+            sp.bounds = p.bounds;
+            sp.block_table = p.block_table;
+            sp.seq_lens = p.seq_lens;
+            sp.budget = p.budget;
+            sp.q = p.q;
+            sp.selected = p.selected;
+            sp.scores_out = p.scores_out;
+            sp.counters = p.counters;
+            sp.status = p.status;
+            sp.num_phys = p.num_phys;
+            sp.Hkv = Hkv;
+            sp.P = P;
+            sp.G = G;
+            sp.Hq = p.Hq;
+            sp.max_pages = p.max_pages;
+            sp.max_budget = p.max_budget;
+            BoxStage stage;
+            stage.buf = sel_buf;
+            stage.bar = sel_bar;
+            stage.phys = sel_phys;
+            stage.slots_per_warp = kSelSlotsPerWarp;
+            stage.wait_limit_ns = p.wait_limit_ns;
+            uint32_t phase_bits = 0;    // parity of this warp's staging slots
+            auto run_unit = [&](int u) {
+                select_unit<T, D, MMA, GMAX>(grp, sp, u, sel_sc, *sel_x, MMA ? &stage : nullptr, &phase_bits);
+                __threadfence();
+                grp.sync();                      // every id of the row is stored
+                if (grp.tid == 0) st_release_gpu(&p.ready[u], 1);
+            };
+            if (n_loc > 0) {
+                int b, h, j, cnt;
+                long long us;
+                locate(g1 - 1, b, h, j, us, cnt);
+                const int u_last = b * Hkv + h;
+                if (us >= g0) run_unit(u_last);
+                locate(g0, b, h, j, us, cnt);
+                int u = b * Hkv + h + (us < g0 ? 1 : 0);   // skip a unit begun in an earlier range
+                for (; u < u_last; ++u) {        // units strictly inside the range
+                    const int ub = u / Hkv;
+                    if (prefix[ub + 1] == prefix[ub]) continue;   // no pages: handled above
+                    run_unit(u);
+                }
+            }
+            return;
+        }
+    }
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // Pages are handled in batches of WB <= min(32, S): the lanes resolve one
@@ -231,21 +317,44 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         // Lookups are software-pipelined over batches: the kept-id load of batch
         // k+2 and the block-table load of batch k+1 are in flight while batch k
         // is issued, so their latency hides behind the ring instead of stalling it.
-        struct Look { int page, phys, b, h; bool active, ok; };
-        auto look_a = [&](long long bb, Look &lk) {      // locate; load the kept id
+        // A lookup moves through stages: 0 located, kept id not read yet (the
+        // single-launch kernel reads it only once the unit's selection is
+        // published); 1 id read; 2 block-table entry read, or nothing to do.
+        struct Look { int page, phys, b, h, j, stage; bool active, ok; };
+        int seen_ready = -1;   // the last unit this lane saw published (acquired once)
+        auto read_id = [&](Look &lk) {                   // stage 0 -> 1 when the id is available
+            const size_t u = (size_t)lk.b * Hkv + lk.h;
+            if (p.dense) {
+                lk.page = lk.j;
+            } else if constexpr (FUSED) {
+                if ((int)u != seen_ready) {
+                    if (ld_acquire_gpu(&p.ready[u]) == 0) return;
+                    seen_ready = (int)u;
+                }
+                lk.page = __ldcg(&p.selected[u * p.max_budget + lk.j]);
+            } else {
+                lk.page = p.selected[u * p.max_budget + lk.j];
+            }
+            lk.stage = 1;
+        };
+        auto look_a = [&](long long bb, Look &lk) {      // locate; read the kept id
             const long long pos = bb + lane;
             lk.active = lane < WB && pos < n_loc;
             lk.ok = false;
-            lk.page = -1; lk.phys = -1; lk.b = 0; lk.h = 0;
+            lk.page = -1; lk.phys = -1; lk.b = 0; lk.h = 0; lk.j = 0;
+            lk.stage = 2;
             if (lk.active) {
-                int j, cnt;
+                int cnt;
                 long long us;
-                locate(rot(pos), lk.b, lk.h, j, us, cnt);
-                lk.page = p.dense ? j : p.selected[((size_t)lk.b * Hkv + lk.h) * p.max_budget + j];
+                locate(rot(pos), lk.b, lk.h, lk.j, us, cnt);
+                lk.stage = 0;
+                read_id(lk);
             }
         };
-        auto look_b = [&](Look &lk) {                    // check the id; load the block-table entry
-            if (!lk.active) return;
+        auto look_b = [&](Look &lk) {                    // check the id; read the block-table entry
+            if (lk.stage == 0) read_id(lk);
+            if (lk.stage != 1) return;
+            lk.stage = 2;
             const int N = (lens[lk.b] + P - 1) / P;
             if (lk.page < 0 || lk.page >= N) {
                 if (p.status) atomicOr(p.status, QASA_DEVERR_SELECTED);
@@ -254,12 +363,43 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             lk.ok = true;
             lk.phys = p.block_table[(size_t)lk.b * p.max_pages + lk.page];
         };
+        // Complete a lookup that is about to be issued.  In the single-launch
+        // kernel this waits (bounded) for the selection of every lane's unit.
+        auto finish = [&](Look &lk) -> bool {
+            if constexpr (FUSED) {
+                uint64_t t_begin = 0;
+                for (int spin = 0;; ++spin) {
+                    if (lk.stage == 0) read_id(lk);
+                    if (!__any_sync(0xffffffffu, lk.stage == 0)) break;
+                    int stop = 0;
+                    if (lane == 0 && (spin & 15) == 15) {
+                        const uint64_t now = global_timer_ns();
+                        if (t_begin == 0) t_begin = now;
+                        else if (now - t_begin > p.wait_limit_ns || *abort_flag) stop = 1;
+                    }
+                    if (__shfl_sync(0xffffffffu, stop, 0)) {
+                        if (lane == 0) {
+                            if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        return false;
+                    }
+                    __nanosleep(128);
+                }
+            }
+            look_b(lk);
+            return true;
+        };
         Look la, lb, lc;
         look_a(0, la);
         look_b(la);
         look_a(WB, lb);
         for (long long base = 0; base < n_loc && !aborted; base += WB) {
             const int nb = (int)min((long long)WB, n_loc - base);
+            if (!finish(la)) {
+                aborted = true;
+                break;
+            }
             int nvalid = 0, row = 0;
             const int page = la.page;
             if (la.active && la.ok) {                    // check the physical page
@@ -720,18 +860,20 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
 
 // ------------------------------------------------------------------ launch
 
-template <typename T, int D, int P, bool MMA, int GMAX>
+template <typename T, int D, int P, bool MMA, int GMAX, bool FUSED>
 static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p0,
                                  int grid, size_t smem_budget, bool pdl, cudaStream_t stream) {
-    constexpr int NW = 8;
+    // The single-launch kernel adds 4 selector warps; one consumer warp fewer
+    // keeps its registers per thread at the two-kernel level.
+    constexpr int NW = FUSED ? 7 : 8;
     constexpr int STAGE = 2 * P * D * (int)sizeof(T);
     AttnParams p = p0;
-    // Pick the number of working consumer warps (4..NW-1) that allows the deepest ring
+    // Pick the number of working consumer warps (up to NW-1) that allows the deepest ring
     // whose depth is a multiple of it (each stage owned by one consumer warp).
     const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int);
     int stages = 0, consumers = 0;
     for (int nw = NW - 1; nw >= 1; --nw) {   // the last consumer warp is the combiner
-        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B);
+        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);
         if (s > 32) s = 32;
@@ -744,53 +886,70 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     if (stages < 2) return cudaErrorInvalidConfiguration;
     p.stages = stages;
     p.consumers = consumers;
-    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B);
-    auto kern = attn_kernel<T, D, P, MMA, GMAX, NW>;
+    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B, FUSED, p.max_pages);
+    auto kern = attn_kernel<T, D, P, MMA, GMAX, NW, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(32 * (NW + 1));
+    cfg.blockDim = dim3(32 * (NW + 1) + (FUSED ? kSelThreads : 0));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (FUSED) {
+        // CTAs wait (bounded) for selections made by other CTAs: ask for a
+        // launch in which every CTA is resident at once
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = (FUSED || pdl) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, km, vm, p);
 }
 
-template <typename T, int D, int P>
+template <typename T, int D, int P, bool FUSED>
 static cudaError_t launch_attn_dp(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p,
                                   int grid, size_t smem_budget, bool pdl, cudaStream_t stream) {
     if constexpr (sizeof(T) == 2) {
         // tensor cores when the query group makes q.K a real contraction
-        if (p.G >= 2) return launch_attn_t<T, D, P, true, 8>(km, vm, p, grid, smem_budget, pdl, stream);
-        return launch_attn_t<T, D, P, false, 1>(km, vm, p, grid, smem_budget, pdl, stream);
+        if (p.G >= 2) return launch_attn_t<T, D, P, true, 8, FUSED>(km, vm, p, grid, smem_budget, pdl, stream);
+        return launch_attn_t<T, D, P, false, 1, FUSED>(km, vm, p, grid, smem_budget, pdl, stream);
     } else {
-        return launch_attn_t<T, D, P, false, 8>(km, vm, p, grid, smem_budget, pdl, stream);
+        return launch_attn_t<T, D, P, false, 8, FUSED>(km, vm, p, grid, smem_budget, pdl, stream);
     }
 }
 
-template <typename T>
+template <typename T, bool FUSED>
 static cudaError_t launch_attn_dt(int D, int P, const CUtensorMap &km, const CUtensorMap &vm,
                                   const AttnParams &p, int grid, size_t smem_budget, bool pdl,
                                   cudaStream_t stream) {
     if (D == 64)
-        return P == 16 ? launch_attn_dp<T, 64, 16>(km, vm, p, grid, smem_budget, pdl, stream)
-                       : launch_attn_dp<T, 64, 32>(km, vm, p, grid, smem_budget, pdl, stream);
-    return P == 16 ? launch_attn_dp<T, 128, 16>(km, vm, p, grid, smem_budget, pdl, stream)
-                   : launch_attn_dp<T, 128, 32>(km, vm, p, grid, smem_budget, pdl, stream);
+        return P == 16 ? launch_attn_dp<T, 64, 16, FUSED>(km, vm, p, grid, smem_budget, pdl, stream)
+                       : launch_attn_dp<T, 64, 32, FUSED>(km, vm, p, grid, smem_budget, pdl, stream);
+    return P == 16 ? launch_attn_dp<T, 128, 16, FUSED>(km, vm, p, grid, smem_budget, pdl, stream)
+                   : launch_attn_dp<T, 128, 32, FUSED>(km, vm, p, grid, smem_budget, pdl, stream);
 }
 
 cudaError_t launch_attention(qasa_dtype dt, int D, int P, const CUtensorMap &km,
                              const CUtensorMap &vm, const AttnParams &p, int grid,
                              size_t smem_budget, bool pdl, cudaStream_t stream) {
     switch (dt) {
-    case QASA_DTYPE_F32: return launch_attn_dt<float>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
-    case QASA_DTYPE_F16: return launch_attn_dt<__half>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
-    default: return launch_attn_dt<__nv_bfloat16>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
+    case QASA_DTYPE_F32: return launch_attn_dt<float, false>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
+    case QASA_DTYPE_F16: return launch_attn_dt<__half, false>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
+    default: return launch_attn_dt<__nv_bfloat16, false>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
+    }
+}
+
+cudaError_t launch_fused_decode(qasa_dtype dt, int D, int P, const CUtensorMap &km,
+                                const CUtensorMap &vm, const AttnParams &p, int grid,
+                                size_t smem_budget, cudaStream_t stream) {
+    switch (dt) {
+    case QASA_DTYPE_F32: return launch_attn_dt<float, true>(D, P, km, vm, p, grid, smem_budget, false, stream);
+    case QASA_DTYPE_F16: return launch_attn_dt<__half, true>(D, P, km, vm, p, grid, smem_budget, false, stream);
+    default: return launch_attn_dt<__nv_bfloat16, true>(D, P, km, vm, p, grid, smem_budget, false, stream);
     }
 }
 

@@ -40,7 +40,7 @@ struct AttnParams {
     const int32_t *block_table;
     const int32_t *seq_lens;
     const int32_t *budget;
-    const int32_t *selected;
+    int32_t *selected;       // read; written too by the single-launch kernel
     const void *q;
     void *out;
     float *part_o;     // [(units + C) * G * D]
@@ -54,6 +54,10 @@ struct AttnParams {
     int stages;        // ring depth, a multiple of `consumers`
     int consumers;     // consumer warps that take pages (<= the compiled count)
     unsigned long long wait_limit_ns;
+    // single-launch decode only: the selection inputs and outputs
+    const void *bounds;
+    float *scores_out;
+    int32_t *ready;    // [units] 1 once a unit's kept ids are published (zero at launch)
 };
 
 struct MassParams {
@@ -93,6 +97,10 @@ cudaError_t launch_select(qasa_dtype dt, int D, const SelectParams &p, int units
 cudaError_t launch_attention(qasa_dtype dt, int D, int P, const CUtensorMap &km, const CUtensorMap &vm,
                              const AttnParams &p, int grid, size_t smem_budget, bool pdl,
                              cudaStream_t stream);
+// One launch for the whole decode step (scoring, selection, attention);
+// cooperative, grid = one CTA per SM.
+cudaError_t launch_fused_decode(qasa_dtype dt, int D, int P, const CUtensorMap &km, const CUtensorMap &vm,
+                                const AttnParams &p, int grid, size_t smem_budget, cudaStream_t stream);
 
 cudaError_t launch_rebuild_bounds(qasa_dtype dt, int D, const RebuildParams &p, int batch,
                                   cudaStream_t stream);
