@@ -33,8 +33,8 @@ def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so next to it (plain gcc, -O2, no CUDA)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp,
-                               _SRC, "-lm"])
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -56,6 +56,13 @@ def _load():
                 _D, _D, _D, _D, _D, ctypes.c_int, ctypes.c_double, _D, _I, _D]
             lib.oracle_decode_unit.restype = ctypes.c_int
             lib.oracle_page_attention_mass.argtypes = [ctypes.c_int] * 4 + [_D, _D, ctypes.c_double, _D]
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_ubyte]
+            lib.oracle_e4m3_decode.restype = ctypes.c_float
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_ubyte
+            _F = ctypes.POINTER(ctypes.c_float)
+            _U = ctypes.POINTER(ctypes.c_ubyte)
+            lib.oracle_fp8_append_replay.argtypes = [ctypes.c_int] * 3 + [_F, ctypes.c_int, _I, _U, _F, _U, _U]
             _lib = lib
     return _lib
 
@@ -192,6 +199,58 @@ def page_hit_rate(mass, selected, k: int) -> Tuple[int, float, float]:
     in_top = np.zeros(len(mass), dtype=bool)
     in_top[top] = True
     return int(in_top[sel].sum()), float(mass[sel].sum()), float(mass[top].sum())
+
+
+# ------------------------------------------------------------------ FP8 KV
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (float32) of E4M3 codes."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    table = np.array([lib.oracle_e4m3_decode(i) for i in range(256)], dtype=np.float32)
+    return table[c]
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, finite overflow saturates, -0 -> +0)."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    flat, of = x.reshape(-1), out.reshape(-1)
+    for i in range(flat.size):
+        of[i] = lib.oracle_e4m3_encode(float(flat[i]))
+    return out
+
+
+def fp8_append_replay(X, P: int, chunk_lens: Sequence[int]):
+    """Quantized appends of one (sequence, KV head) tensor X [L, d] (fp32
+    values), chunk by chunk.  Returns (codes [L, d] uint8, amax [N] float32,
+    lo [N, d] uint8, hi [N, d] uint8)."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    L, d = X.shape
+    N = num_pages(L, P)
+    ch = _i32(chunk_lens)
+    codes = np.zeros((max(L, 1), d), dtype=np.uint8)
+    amax = np.zeros(max(N, 1), dtype=np.float32)
+    lo = np.zeros((max(N, 1), d), dtype=np.uint8)
+    hi = np.zeros((max(N, 1), d), dtype=np.uint8)
+    F = ctypes.POINTER(ctypes.c_float)
+    U = ctypes.POINTER(ctypes.c_ubyte)
+    _load().oracle_fp8_append_replay(int(L), int(d), int(P), X.ctypes.data_as(F), len(ch),
+                                     _ip(ch if len(ch) else np.zeros(1, np.int32)),
+                                     codes.ctypes.data_as(U), amax.ctypes.data_as(F),
+                                     lo.ctypes.data_as(U), hi.ctypes.data_as(U))
+    return codes[:L].copy(), amax[:N].copy(), lo[:N].copy(), hi[:N].copy()
+
+
+def fp8_scale(amax) -> np.ndarray:
+    """Per-page scale amax / 448 as the fp32 division computes it."""
+    return (np.asarray(amax, dtype=np.float32) / np.float32(448.0)).astype(np.float32)
+
+
+def fp8_dequant(codes, scale_per_row) -> np.ndarray:
+    """Exact values code * s (float64: a 4-bit times a 24-bit significand)."""
+    return e4m3_decode(codes).astype(np.float64) * np.asarray(scale_per_row, dtype=np.float64)[..., None]
 
 
 def run_units(fn, items, threads: int = 1):

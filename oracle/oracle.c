@@ -230,3 +230,120 @@ void oracle_page_attention_mass(int G, int d, int L, int P, const double *q, con
     }
     free(z);
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 KV cache (e4m3 codes with a per-(page, KV head) scale).
+ *
+ * The TinyServe summary lists support for different KV formats among the
+ * system's features without details; the readings here are: K and V are stored
+ * as FP8 E4M3 codes (OCP 8-bit floating point, E4M3: 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits, subnormals, no infinities, S.1111.111 = NaN,
+ * largest finite 448); every (page, KV head) keeps amax = the largest |x| of
+ * the K (resp. V) values written into it, and scale s = amax / 448 (fp32); a
+ * value x is stored as code(x / s); the page box holds the minimum and maximum
+ * codes per channel (exact: every key of the page shares s).  When an append
+ * raises a page's amax, the codes already in the page are re-quantized to the
+ * new scale: code(dec(c) * s_old / s_new).  Those steps are fp32 operations
+ * (each rounded to nearest), which this code performs in C float.
+ * ---------------------------------------------------------------------- */
+
+/* Value of an E4M3 code (NaN for S.1111.111). */
+float oracle_e4m3_decode(unsigned char c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);                 /* subnormal: m * 2^-6 / 8 */
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return (float)(sign ? -v : v);
+}
+
+/* Nearest E4M3 code, ties to the even mantissa; finite values beyond 448
+ * saturate to +-448; zero (of either sign) gives +0; NaN gives 0x7F. */
+unsigned char oracle_e4m3_encode(float xf)
+{
+    double x = xf, a;
+    int sign, e;
+    double q, fl;
+    long mant;
+    if (x != x) return 0x7F;
+    sign = x < 0;
+    a = fabs(x);
+    if (a > 448.0) return (unsigned char)((sign << 7) | 0x7E);
+    if (a < ldexp(1.0, -6)) {                             /* subnormal range, step 2^-9 */
+        q = a * 512.0;
+        fl = floor(q);
+        mant = (long)fl;
+        if (q - fl > 0.5 || (q - fl == 0.5 && (mant & 1))) ++mant;
+        if (mant == 0) return 0;                          /* +0 for both signs */
+        if (mant == 8) return (unsigned char)((sign << 7) | (1 << 3));
+        return (unsigned char)((sign << 7) | mant);
+    }
+    e = (int)floor(log2(a));
+    if (ldexp(1.0, e) > a) --e;                           /* guard log2 rounding */
+    if (ldexp(1.0, e + 1) <= a) ++e;
+    q = (a / ldexp(1.0, e) - 1.0) * 8.0;                  /* exact: 0 <= q < 8 */
+    fl = floor(q);
+    mant = (long)fl;
+    if (q - fl > 0.5 || (q - fl == 0.5 && (mant & 1))) ++mant;
+    if (mant == 8) { mant = 0; ++e; }
+    if (e > 8 || (e == 8 && mant > 6)) return (unsigned char)((sign << 7) | 0x7E);
+    return (unsigned char)((sign << 7) | ((e + 7) << 3) | (int)mant);
+}
+
+/* Quantize one value with scale s (fp32); s == 0 stores 0. */
+static unsigned char fp8_quant(float x, float s)
+{
+    if (s == 0.0f) return 0;
+    return oracle_e4m3_encode(x / s);
+}
+
+/* Replay the quantized appends of ONE (sequence, KV head) tensor (K or V):
+ * X [L][d] holds the input values (fp32), appended in chunks of chunk_lens
+ * (summing to L).  Outputs: codes [L][d], amax [N], and per page the minimum
+ * and maximum codes per channel lo, hi [N][d] (by value; compare the codes of
+ * K, ignore for V). */
+void oracle_fp8_append_replay(int L, int d, int P, const float *X, int nchunks, const int *chunk_lens,
+                              unsigned char *codes, float *amax, unsigned char *lo, unsigned char *hi)
+{
+    int N = num_pages_of(L, P), t0 = 0;
+    for (int p = 0; p < N; ++p) amax[p] = 0.0f;
+    for (int k = 0; k < nchunks && t0 < L; ++k) {
+        int t1 = t0 + chunk_lens[k];
+        if (t1 > L) t1 = L;
+        for (int p = t0 / P; p * P < t1; ++p) {
+            int ts = t0 > p * P ? t0 : p * P;
+            int te = t1 < (p + 1) * P ? t1 : (p + 1) * P;
+            int fresh = (ts == p * P);
+            float old = fresh ? 0.0f : amax[p], m = old;
+            for (int t = ts; t < te; ++t)
+                for (int c = 0; c < d; ++c) {
+                    float v = fabsf(X[(size_t)t * d + c]);
+                    if (v > m) m = v;
+                }
+            float s_old = old / 448.0f, s_new = m / 448.0f;
+            if (!fresh && m > old)
+                for (int t = p * P; t < ts; ++t)
+                    for (int c = 0; c < d; ++c) {
+                        unsigned char *cc = &codes[(size_t)t * d + c];
+                        float x = oracle_e4m3_decode(*cc) * s_old;
+                        *cc = fp8_quant(x, s_new);
+                    }
+            for (int t = ts; t < te; ++t)
+                for (int c = 0; c < d; ++c)
+                    codes[(size_t)t * d + c] = fp8_quant(X[(size_t)t * d + c], s_new);
+            amax[p] = m;
+            for (int c = 0; c < d; ++c) {
+                unsigned char mn = codes[(size_t)(p * P) * d + c], mx = mn;
+                for (int t = p * P + 1; t < te; ++t) {
+                    unsigned char v = codes[(size_t)t * d + c];
+                    if (oracle_e4m3_decode(v) < oracle_e4m3_decode(mn)) mn = v;
+                    if (oracle_e4m3_decode(v) > oracle_e4m3_decode(mx)) mx = v;
+                }
+                lo[(size_t)p * d + c] = mn;
+                hi[(size_t)p * d + c] = mx;
+            }
+        }
+        t0 = t1;
+    }
+}

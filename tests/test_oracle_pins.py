@@ -331,3 +331,108 @@ def test_hit_rate_against_brute_force_subsets():
         top = min((s for s in subsets if abs(sum(mass[list(s)]) - best_sum) < 1e-15),
                   key=lambda s: sorted((-mass[i], i) for i in s))
         assert hits == len(set(top) & set(sel.tolist()))
+
+
+# ------------------------------------------------------------- FP8 KV (E4M3)
+# Format: OCP 8-bit floating point, E4M3 variant (bias 7, 3 mantissa bits,
+# subnormals, no infinities, S.1111.111 = NaN, largest finite 448).
+
+def test_e4m3_decode_known_codes_and_order():
+    d = oracle.e4m3_decode(np.arange(256))
+    known = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125,
+             0x3F: 1.875, 0x40: 2.0, 0x77: 240.0, 0x78: 256.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in known.items():
+        assert d[c] == v, hex(c)
+    assert np.isnan(d[0x7F]) and np.isnan(d[0xFF])
+    pos = d[:0x7F]
+    assert np.all(np.diff(pos) > 0), "codes 0..126 must increase"
+    assert np.array_equal(d[0x80:0xFF], -pos)
+
+
+def test_e4m3_encode_is_the_nearest_code_with_ties_to_even():
+    d = oracle.e4m3_decode(np.arange(256)).astype(np.float64)
+    finite = [c for c in range(256) if not np.isnan(d[c]) and c != 0x80]
+    r = rng(40)
+    xs = np.concatenate([r.standard_normal(3000) * 10.0 ** r.uniform(-4, 3, 3000),
+                         (d[1:0x7E] + d[2:0x7F]) / 2,          # midpoints between neighbours
+                         -(d[1:0x7E] + d[2:0x7F]) / 2])
+    xs = xs.astype(np.float32)
+    got = oracle.e4m3_encode(xs)
+    for x, c in zip(xs.astype(np.float64), got):
+        if abs(x) > 448:
+            assert d[c] == np.sign(x) * 448
+            continue
+        err = np.abs(d[finite] - x)
+        best = err.min()
+        cands = [finite[i] for i in np.flatnonzero(err == best)]
+        if len(cands) > 1:      # a tie: the code with the even mantissa (a zero result is +0)
+            cands = [k for k in cands if (k & 1) == 0 or d[k] == 0]
+        assert c in cands, (x, c, cands)
+
+
+def test_e4m3_round_trip_saturation_and_zero():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF, 0x80)], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+    assert oracle.e4m3_encode(np.float32([-0.0, -1e-30, 1e30, -1e30, 449.0]))[:5].tolist() == [0, 0, 0x7E, 0xFE, 0x7E]
+
+
+def _fp8_page_check(X, P, codes, amax, lo, hi):
+    L, d = X.shape
+    for p in range(-(-L // P)):
+        rows = slice(p * P, min(L, (p + 1) * P))
+        assert amax[p] == np.abs(X[rows]).max()
+        v = oracle.e4m3_decode(codes[rows])
+        assert np.array_equal(oracle.e4m3_decode(lo[p]), v.min(axis=0))
+        assert np.array_equal(oracle.e4m3_decode(hi[p]), v.max(axis=0))
+
+
+def test_fp8_append_single_chunk_is_direct_quantization():
+    r = rng(41)
+    P, L, d = 16, 75, 8
+    X = (r.standard_normal((L, d)) * 3).astype(np.float32)
+    codes, amax, lo, hi = oracle.fp8_append_replay(X, P, [L])
+    for p in range(-(-L // P)):
+        rows = slice(p * P, min(L, (p + 1) * P))
+        s = np.float32(np.abs(X[rows]).max()) / np.float32(448.0)
+        assert np.array_equal(codes[rows], oracle.e4m3_encode(X[rows] / s))
+    _fp8_page_check(X, P, codes, amax, lo, hi)
+
+
+def test_fp8_append_without_amax_growth_matches_one_chunk():
+    # the first token of every page holds the page's largest |x|: later chunks
+    # never change a scale, so the chunking cannot matter
+    r = rng(42)
+    P, L, d = 16, 64, 8
+    X = (r.standard_normal((L, d))).astype(np.float32)
+    X[::P, 0] = 100.0
+    one = oracle.fp8_append_replay(X, P, [L])
+    many = oracle.fp8_append_replay(X, P, [1] * L)
+    for a, b in zip(one, many):
+        assert np.array_equal(a, b)
+
+
+def test_fp8_append_requantizes_when_amax_grows():
+    # token by token with growing magnitudes: the old codes are re-scaled, so
+    # the error of every value stays within two rounding steps of the final
+    # scale (one for its own quantization, one per re-scaling is bounded by the
+    # geometric growth here); leaving the old codes alone would be off by the
+    # ratio of the scales
+    r = rng(43)
+    P, L, d = 16, 48, 4
+    X = (r.standard_normal((L, d)) * np.linspace(1, 40, L)[:, None]).astype(np.float32)
+    codes, amax, lo, hi = oracle.fp8_append_replay(X, P, [1] * L)
+    _fp8_page_check(X, P, codes, amax, lo, hi)
+    for p in range(L // P):
+        rows = slice(p * P, (p + 1) * P)
+        s = np.float64(np.float32(amax[p]) / np.float32(448.0))
+        deq = oracle.e4m3_decode(codes[rows]).astype(np.float64) * s
+        x = X[rows].astype(np.float64)
+        # half an E4M3 step at |x| is at most |x| / 16 (normal) or s * 2^-10 (subnormal)
+        step = np.maximum(np.abs(x) / 16.0, s * 2.0 ** -10)
+        assert np.all(np.abs(deq - x) <= 4 * step + 1e-12), np.max(np.abs(deq - x) / step)
+
+
+def test_fp8_append_zero_page():
+    X = np.zeros((20, 4), np.float32)
+    codes, amax, lo, hi = oracle.fp8_append_replay(X, 16, [3, 17])
+    assert not codes.any() and not amax.any() and not lo.any() and not hi.any()
