@@ -61,7 +61,8 @@ extern "C" {
 typedef enum {
     QASA_DTYPE_F32 = 0,
     QASA_DTYPE_F16 = 1,
-    QASA_DTYPE_BF16 = 2
+    QASA_DTYPE_BF16 = 2,
+    QASA_DTYPE_E4M3 = 3        /* FP8 KV codes with per-(page, KV head) scales; q, out, k_new, v_new are f16 */
 } qasa_dtype;
 
 typedef enum {
@@ -93,7 +94,25 @@ typedef struct {
     int32_t page_size;
     int32_t head_dim;
     qasa_dtype dtype;
+    float *page_scales;      /* QASA_DTYPE_E4M3 only: [num_phys_pages][num_kv_heads][4] =
+                                (amax of K, amax of V, unused, unused); NULL otherwise */
 } qasa_kv_cache;
+
+/*
+ * FP8 KV (QASA_DTYPE_E4M3; the TinyServe summary lists support for several KV
+ * formats).  k_pool, v_pool and page_bounds hold FP8 E4M3 codes (OCP 8-bit
+ * floating point: bias 7, 3 mantissa bits, largest finite 448).  Every
+ * (page, KV head) keeps amax, the largest |x| of the K (resp. V) values written
+ * into it, and the scale s = amax / 448 (fp32 division): a value x is stored as
+ * code(x / s) (round to nearest even, saturating, zero stored as +0; s = 0
+ * stores 0), and its value is code * s.  When an append raises a page's amax,
+ * the codes already in the page are re-quantized to the new scale,
+ * code(value(c) * s_old / s_new) in fp32, so the page keeps one scale.  The box
+ * holds the per-channel minimum and maximum K codes of the page: exact bounds of
+ * the dequantized keys, since they share the page's scale.  Scores and
+ * attention use code * s.  page_scales entries start at any value: a page's
+ * first append (the one writing slot 0) sets them.
+ */
 
 /*
  * Append new tokens to every sequence and keep the page boxes current

@@ -20,6 +20,7 @@ if not os.path.exists(_LIB_PATH):
 _lib = ctypes.CDLL(_LIB_PATH)
 
 DTYPE_IDS = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+E4M3 = 3            # FP8 KV: uint8 pools and boxes holding E4M3 codes, plus page_scales
 STATUS_OK = 0
 
 DEVERR = {
@@ -36,7 +37,8 @@ class _Cache(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
                 ("page_bounds", ctypes.c_void_p), ("num_phys_pages", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("page_scales", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -119,32 +121,47 @@ class PagedKVCache:
 
     k_pool, v_pool : [num_phys_pages, num_kv_heads, page_size, head_dim]
     page_bounds    : [num_phys_pages, num_kv_heads, 2, head_dim]  (lo row, hi row)
+    page_scales    : FP8 KV only (uint8 pools holding E4M3 codes):
+                     [num_phys_pages, num_kv_heads, 4] float32 (amax of K, amax of V, -, -);
+                     queries, outputs and appended K/V are then float16
     """
 
-    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, page_bounds: torch.Tensor):
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, page_bounds: torch.Tensor,
+                 page_scales: Optional[torch.Tensor] = None):
         if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
             raise ValueError("k_pool and v_pool must share a 4-d shape")
         n, hkv, p, d = k_pool.shape
         if tuple(page_bounds.shape) != (n, hkv, 2, d):
             raise ValueError("page_bounds must be [num_phys_pages, num_kv_heads, 2, head_dim]")
-        if not (k_pool.dtype == v_pool.dtype == page_bounds.dtype) or k_pool.dtype not in DTYPE_IDS:
-            raise ValueError("pools must share one of float32 / float16 / bfloat16")
+        fp8 = k_pool.dtype == torch.uint8
+        if not (k_pool.dtype == v_pool.dtype == page_bounds.dtype) or not (fp8 or k_pool.dtype in DTYPE_IDS):
+            raise ValueError("pools must share one of float32 / float16 / bfloat16 / uint8 (E4M3 codes)")
+        if fp8:
+            if page_scales is None or tuple(page_scales.shape) != (n, hkv, 4) or page_scales.dtype != torch.float32:
+                raise ValueError("FP8 pools need page_scales [num_phys_pages, num_kv_heads, 4] float32")
+            _contig(page_scales, "page_scales")
         for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool"), (page_bounds, "page_bounds")):
             _contig(t, nm)
         self.k_pool, self.v_pool, self.page_bounds = k_pool, v_pool, page_bounds
+        self.page_scales = page_scales if fp8 else None
         self.num_phys_pages, self.num_kv_heads, self.page_size, self.head_dim = n, hkv, p, d
         self.dtype = k_pool.dtype
+        self.is_fp8 = fp8
         self._c = _Cache(k_pool.data_ptr(), v_pool.data_ptr(), page_bounds.data_ptr(), n, hkv, p,
-                         d, DTYPE_IDS[k_pool.dtype])
+                         d, E4M3 if fp8 else DTYPE_IDS[k_pool.dtype],
+                         page_scales.data_ptr() if fp8 else None)
 
     @classmethod
     def empty(cls, num_phys_pages: int, num_kv_heads: int, page_size: int, head_dim: int,
               dtype=torch.float16, device="cuda") -> "PagedKVCache":
+        """dtype float32 / float16 / bfloat16, or torch.uint8 for FP8 (E4M3) KV."""
         shape = (num_phys_pages, num_kv_heads, page_size, head_dim)
+        scales = (torch.zeros((num_phys_pages, num_kv_heads, 4), dtype=torch.float32, device=device)
+                  if dtype == torch.uint8 else None)
         return cls(torch.empty(shape, dtype=dtype, device=device),
                    torch.empty(shape, dtype=dtype, device=device),
                    torch.empty((num_phys_pages, num_kv_heads, 2, head_dim), dtype=dtype,
-                               device=device))
+                               device=device), scales)
 
     @property
     def c_ref(self):

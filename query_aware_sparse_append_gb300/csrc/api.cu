@@ -19,12 +19,15 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s: far beyond 
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t elem_size(qasa_dtype dt) { return dt == QASA_DTYPE_F32 ? 4 : 2; }
+size_t elem_size(qasa_dtype dt) { return dt == QASA_DTYPE_F32 ? 4 : dt == QASA_DTYPE_E4M3 ? 1 : 2; }
 
 qasa_status check_cache(const qasa_kv_cache *c) {
     if (!c || !c->k_pool || !c->v_pool || !c->page_bounds) return QASA_ERR_NULL;
-    if (c->dtype != QASA_DTYPE_F32 && c->dtype != QASA_DTYPE_F16 && c->dtype != QASA_DTYPE_BF16)
+    if (c->dtype != QASA_DTYPE_F32 && c->dtype != QASA_DTYPE_F16 && c->dtype != QASA_DTYPE_BF16 &&
+        c->dtype != QASA_DTYPE_E4M3)
         return QASA_ERR_DTYPE;
+    if (c->dtype == QASA_DTYPE_E4M3 && !c->page_scales) return QASA_ERR_NULL;
+    if (c->dtype == QASA_DTYPE_E4M3 && !aligned16(c->page_scales)) return QASA_ERR_ALIGN;
     if (c->head_dim != 64 && c->head_dim != 128) return QASA_ERR_SHAPE;
     if (c->page_size != 16 && c->page_size != 32) return QASA_ERR_SHAPE;
     if (c->num_kv_heads < 1 || c->num_phys_pages < 1) return QASA_ERR_SHAPE;
@@ -131,6 +134,17 @@ qasa_status pool_tensor_map(CUtensorMap *map, void *base, const qasa_kv_cache *c
                                   : c->dtype == QASA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint64_t rows = (cuuint64_t)c->num_phys_pages * c->num_kv_heads * c->page_size;
+    if (c->dtype == QASA_DTYPE_E4M3) {
+        // FP8 codes: one unswizzled box of head_dim bytes x page_size rows per tile
+        cuuint64_t dims[2] = {(cuuint64_t)c->head_dim, rows};
+        cuuint64_t strides[1] = {(cuuint64_t)c->head_dim};
+        cuuint32_t box[2] = {(cuuint32_t)c->head_dim, (cuuint32_t)c->page_size};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r8 = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        return r8 == CUDA_SUCCESS ? QASA_OK : QASA_ERR_DRIVER;
+    }
     const cuuint32_t boxw = (cuuint32_t)(128 / es);
     const cuuint32_t nsub = (cuuint32_t)(c->head_dim * es / 128);
     CUresult r;
@@ -176,6 +190,7 @@ qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_head
     p.Hq = num_q_heads;
     p.max_pages = max_pages;
     p.max_budget = max_budget;
+    p.scales = cache->page_scales;
     cudaError_t e = launch_select(cache->dtype, cache->head_dim, p, batch * cache->num_kv_heads, stream);
     return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
 }
@@ -246,6 +261,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     p.bounds = cache->page_bounds;
     p.scores_out = scores_out;
     p.ready = reinterpret_cast<int32_t *>(ws + w.counters) + units;
+    p.scales = cache->page_scales;
     size_t budget = smem_optin();
     if (budget == 0) return QASA_ERR_CUDA;
     budget = budget > 1024 ? budget - 1024 : budget;   // leave room for static shared memory
@@ -294,6 +310,7 @@ qasa_status qasa_kv_append(const qasa_kv_cache *cache, const int32_t *block_tabl
     p.P = cache->page_size;
     p.max_pages = max_pages_per_seq;
     p.T = max_new_tokens;
+    p.scales = cache->page_scales;
     cudaError_t e = launch_append(cache->dtype, cache->head_dim, p, batch, stream);
     return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
 }
@@ -398,7 +415,7 @@ qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void 
         !aligned16(workspace))
         return QASA_ERR_WORKSPACE;
     if (batch == 0) return QASA_OK;
-    if (single_launch_enabled()) {
+    if (single_launch_enabled() && cache->dtype != QASA_DTYPE_E4M3) {
         st = run_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
                            max_budget, selected, scale, out, workspace, workspace_bytes, batch,
                            device_status, false, false, stream, true, scores_out);
@@ -439,6 +456,7 @@ qasa_status qasa_page_attention_mass(const qasa_kv_cache *cache, const void *q, 
     if (st != QASA_OK) return st;
     if (!mass) return QASA_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(mass) & 3u) return QASA_ERR_ALIGN;
+    if (cache->dtype == QASA_DTYPE_E4M3) return QASA_ERR_DTYPE;   // measured on 16/32-bit caches
     MassParams p;
     p.k_pool = cache->k_pool;
     p.block_table = block_table;

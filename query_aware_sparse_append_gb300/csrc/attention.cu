@@ -36,6 +36,8 @@
 //
 // Every wait is bounded: a wait that gives up sets QASA_DEVERR_TIMEOUT, the CTA
 // stops issuing, drains the copies it issued (again bounded) and returns.
+#include <type_traits>
+
 #include "select_device.cuh"
 
 namespace qasa {
@@ -53,11 +55,13 @@ constexpr int kSelStageSlots = 4 * kSelSlotsPerWarp;
 
 // Host-side size of the dynamic shared memory (mirrors the device carve-up).
 size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int P, bool mma, int B,
-                       bool fused, int max_pages) {
+                       bool fused, int max_pages, bool fp8 = false) {
     size_t s = 1024;                                   // alignment slack for the ring
     s += (size_t)stages * stage_bytes;
     s += (size_t)stages * 2 * sizeof(uint64_t);        // full / empty barriers
     s += (size_t)stages * (sizeof(StageInfo) + sizeof(int));
+    if (fp8) s += 16 + (size_t)stages * 16;            // per-stage page scales
+    if (fp8) s += 1024 + (size_t)nw * 2 * P * D * 2;   // per-warp half copies of the K and V tiles
     s += (size_t)nw * gmax * (D + 2) * sizeof(float);  // combine scratch
     if (!mma) s += (size_t)nw * gmax * (D + P) * sizeof(float);
     s += (size_t)(2 * B + 2) * sizeof(int);            // prefix, lengths
@@ -95,10 +99,13 @@ template <typename T, int D, int P, bool MMA, int GMAX, int NW, bool FUSED>
 __global__ void __launch_bounds__(32 * (NW + 1) + (FUSED ? kSelThreads : 0), 1)
 attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
             AttnParams p) {
-    constexpr int ES = (int)sizeof(T);
+    constexpr bool F8 = is_fp8<T>::value;
+    using MT = typename std::conditional<F8, __half, T>::type;   // q, out and MMA operand type
+    constexpr int ES = F8 ? 1 : (int)sizeof(T);  // bytes per stored KV element
+    constexpr int MES = (int)sizeof(MT);         // bytes per element of the tiles the consumers read
     constexpr int TILE = P * D * ES;            // one (page, head) tile of K or V
     constexpr int STAGE = 2 * TILE;
-    constexpr int NSUB = D * ES / 128;          // 128-byte column boxes per tile
+    constexpr int NSUB = F8 ? 1 : D * ES / 128; // 128-byte column boxes per tile
     constexpr int BOXW = 128 / ES;              // elements per box row
     static_assert(TILE % 1024 == 0, "tile must keep 1024-byte swizzle alignment");
 
@@ -111,7 +118,9 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     uint64_t *empty_bar = full_bar + S;
     StageInfo *info = reinterpret_cast<StageInfo *>(empty_bar + S);
     int *last_ph = reinterpret_cast<int *>(info + S);             // [S] phase of the last copy
-    float *scr_o = reinterpret_cast<float *>(last_ph + S);        // [NWK][GMAX][D]
+    float4 *st_scale = reinterpret_cast<float4 *>(                 // FP8: [S] the page's amax (K, V, -, -)
+        (reinterpret_cast<uintptr_t>(last_ph + S) + 15) & ~uintptr_t(15));
+    float *scr_o = reinterpret_cast<float *>(st_scale + (F8 ? S : 0));   // [NWK][GMAX][D]
     float *scr_m = scr_o + NWK * GMAX * D;                         // [NWK][GMAX]
     float *scr_l = scr_m + NWK * GMAX;                             // [NWK][GMAX]
     float *ff_q = scr_l + NWK * GMAX;                              // FFMA only: [NWK][GMAX][D]
@@ -123,11 +132,17 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     // staging slots with their barriers
     float *sel_sc = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(lens + p.B) + 15) & ~uintptr_t(15));
     SelScratch *sel_x = reinterpret_cast<SelScratch *>(sel_sc + (FUSED ? p.max_pages : 0));
-    int32_t *sel_phys = reinterpret_cast<int32_t *>((reinterpret_cast<uintptr_t>(sel_x + 1) + 15) & ~uintptr_t(15));
+    int32_t *sel_phys = reinterpret_cast<int32_t *>(
+        (reinterpret_cast<uintptr_t>(sel_x + (FUSED ? 1 : 0)) + 15) & ~uintptr_t(15));
     unsigned char *sel_buf = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(sel_phys + (FUSED ? p.max_pages : 0)) + 15) & ~uintptr_t(15));
     constexpr int kSelTileB = 16 * (2 * D * ES + 64);
     uint64_t *sel_bar = reinterpret_cast<uint64_t *>(sel_buf + (FUSED && MMA ? kSelStageSlots * kSelTileB : 0));
+    // FP8: per working warp, half-precision copies of its current K and V tiles
+    // (laid out like a 128-byte-swizzled 16-bit tile, so the MMA path reads them
+    // with the same ldmatrix addressing)
+    unsigned char *f8_scr = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(sel_bar + (FUSED && MMA ? kSelStageSlots : 0)) + 1023) & ~uintptr_t(1023));
     __shared__ int s_abort;      // a bounded wait gave up
     // segment hand-off: [0] completes when the NWK working warps have written
     // their states for a segment; [1] completes when the combiner has read them
@@ -203,8 +218,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             if (prefix[b + 1] != prefix[b]) continue;
             for (int h = 0; h < Hkv; ++h) {
                 if ((b * Hkv + h) % C != c) continue;
-                T *o = static_cast<T *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
-                for (int i = tid; i < G * D; i += blockDim.x) o[i] = elem<T>::from_f(0.f);
+                MT *o = static_cast<MT *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+                for (int i = tid; i < G * D; i += blockDim.x) o[i] = elem<MT>::from_f(0.f);
                 if constexpr (FUSED) {   // and no kept ids
                     int32_t *row = p.selected + ((size_t)b * Hkv + h) * p.max_budget;
                     for (int i = tid; i < p.max_budget; i += blockDim.x) row[i] = -1;
@@ -274,6 +289,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             sp.Hq = p.Hq;
             sp.max_pages = p.max_pages;
             sp.max_budget = p.max_budget;
+            sp.scales = p.scales;
             BoxStage stage;
             stage.buf = sel_buf;
             stage.bar = sel_bar;
@@ -444,8 +460,13 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     info[s_l].nvalid = nvalid;
                     unsigned char *st = ring + (size_t)s_l * STAGE;
                     if (nvalid > 0) {
-                        mbar_arrive_expect_tx(&full_bar[s_l], STAGE);
-                        if (p.one_box) {
+                        mbar_arrive_expect_tx(&full_bar[s_l], STAGE + (F8 ? 16 : 0));
+                        if constexpr (F8) {
+                            // one 2-D box per code tile, and the page's scales (16 bytes)
+                            tma_load_2d(st, &kmap, &full_bar[s_l], 0, row);
+                            tma_load_2d(st + TILE, &vmap, &full_bar[s_l], 0, row);
+                            bulk_load(&st_scale[s_l], p.scales + (size_t)(row / P) * 4, 16, &full_bar[s_l]);
+                        } else if (p.one_box) {
                             tma_load_3d(st, &kmap, &full_bar[s_l], 0, row, 0);
                             tma_load_3d(st + TILE, &vmap, &full_bar[s_l], 0, row, 0);
                         } else {
@@ -539,14 +560,14 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused
             ++kseg;
 
-            T *ob = static_cast<T *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+            MT *ob = static_cast<MT *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
             if (g == us && s1 == ue) {                  // the whole unit is in this CTA
 #pragma unroll
                 for (int hh = 0; hh < GMAX; ++hh) {
                     if (hh >= G) break;
                     const float inv = Lh[hh] > 0.f ? 1.f / Lh[hh] : 0.f;
 #pragma unroll
-                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<T>::from_f(acc[hh][jj] * inv);
+                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<MT>::from_f(acc[hh][jj] * inv);
                 }
                 continue;
             }
@@ -603,7 +624,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     if (hh >= G) break;
                     const float inv = Lh[hh] > 0.f ? 1.f / Lh[hh] : 0.f;
 #pragma unroll
-                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<T>::from_f(acc[hh][jj] * inv);
+                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<MT>::from_f(acc[hh][jj] * inv);
                 }
                 if (lane == 0) p.counters[u] = 0;
             }
@@ -629,7 +650,19 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         locate(g, b, h, j0, us, cnt);
         const long long ue = us + cnt;
         const long long s1 = min(run_end(pos), ue);
-        const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+        const MT *qb = static_cast<const MT *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+        // FP8: turn a code tile into this warp's half copy (rows >= nvalid as zeros)
+        unsigned char *my_k = f8_scr + (size_t)w * 2 * P * D * 2, *my_v = my_k + P * D * 2;
+        auto f8_to_half = [&](const unsigned char *src, unsigned char *dst, int nvalid) {
+            constexpr int CH = D / 16;               // 16-code chunks per row
+            for (int idx = lane; idx < P * CH; idx += 32) {
+                const int r = idx / CH, k = idx % CH;
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                if (r < nvalid) e4m3x16_to_h(*reinterpret_cast<const uint4 *>(src + r * D + k * 16), lo, hi);
+                *reinterpret_cast<uint4 *>(dst + swz128_offset<P>(r, 2 * k)) = lo;
+                *reinterpret_cast<uint4 *>(dst + swz128_offset<P>(r, 2 * k + 1)) = hi;
+            }
+        };
 
         // Page i of the CTA range goes to consumer warp i % NWK and ring stage
         // i % S.  S is a multiple of NWK, so every stage always belongs to the
@@ -650,7 +683,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             for (int ks = 0; ks < D / 16; ++ks) {
                 qf[ks][0] = 0u; qf[ks][1] = 0u;
                 if (nq < G) {
-                    const T *qr = qb + (size_t)nq * D + ks * 16 + 2 * cq;
+                    const MT *qr = qb + (size_t)nq * D + ks * 16 + 2 * cq;
                     qf[ks][0] = *reinterpret_cast<const uint32_t *>(qr);
                     qf[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
                 }
@@ -671,8 +704,21 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 const int nvalid = info[s].nvalid;
                 unsigned char *kst = ring + (size_t)s * STAGE;
                 unsigned char *vst = kst + TILE;
-                const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
-                if (nvalid > 0 && nvalid < P) {
+                uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
+                float zscale = p.scale_log2, vscale = 1.f;
+                if constexpr (F8) {
+                    if (nvalid > 0) {
+                        const float4 am = st_scale[s];
+                        zscale = p.scale_log2 * fp8_scale(am.x);
+                        vscale = fp8_scale(am.y);
+                        f8_to_half(kst, my_k, nvalid);
+                        f8_to_half(vst, my_v, nvalid);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty_bar[s]);   // the codes are copied out: free the stage
+                    kbase = smem_u32(my_k);
+                    vbase = smem_u32(my_v);
+                } else if (nvalid > 0 && nvalid < P) {
                     // rows past the sequence end may hold anything: zero V there so that
                     // the masked (zero) weights cannot meet a NaN in the P.V product
                     const int rows = ((nvalid + 15) & ~15) - nvalid;
@@ -692,15 +738,15 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                         const int chn = 2 * ks + (lane >> 4);
                         uint32_t a[4];
                         ldmatrix_x4(kbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
-                        if (ks & 1) mma16816<T>::run(sb, a, qf[ks][0], qf[ks][1]);
-                        else mma16816<T>::run(sa, a, qf[ks][0], qf[ks][1]);
+                        if (ks & 1) mma16816<MT>::run(sb, a, qf[ks][0], qf[ks][1]);
+                        else mma16816<MT>::run(sa, a, qf[ks][0], qf[ks][1]);
                     }
                     const int t0 = sub * 16 + (lane >> 2), t1 = t0 + 8;
                     const bool v0 = t0 < nvalid, v1 = t1 < nvalid;
-                    const float z0 = v0 ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
-                    const float z1 = v0 ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
-                    const float z2 = v1 ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
-                    const float z3 = v1 ? (sa[3] + sb[3]) * p.scale_log2 : -INFINITY;
+                    const float z0 = v0 ? (sa[0] + sb[0]) * zscale : -INFINITY;
+                    const float z1 = v0 ? (sa[1] + sb[1]) * zscale : -INFINITY;
+                    const float z2 = v1 ? (sa[2] + sb[2]) * zscale : -INFINITY;
+                    const float z3 = v1 ? (sa[3] + sb[3]) * zscale : -INFINITY;
                     float x0 = fmaxf(z0, z2), x1 = fmaxf(z1, z3);
 #pragma unroll
                     for (int off = 4; off < 32; off <<= 1) {
@@ -718,19 +764,20 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     for (int mt = 0; mt < D / 16; ++mt) {
                         o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
                     }
-                    const uint32_t pb0 = movmatrix_trans(mma16816<T>::pack2(p0, p1));
-                    const uint32_t pb1 = movmatrix_trans(mma16816<T>::pack2(p2, p3));
+                    // FP8: the page's V scale rides on the weights (l keeps the plain sum)
+                    const uint32_t pb0 = movmatrix_trans(mma16816<MT>::pack2(p0 * vscale, p1 * vscale));
+                    const uint32_t pb1 = movmatrix_trans(mma16816<MT>::pack2(p2 * vscale, p3 * vscale));
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
                         const int tok = sub * 16 + (lane & 7) + (lane >> 4) * 8;
                         const int chn = 2 * mt + ((lane >> 3) & 1);
                         uint32_t a[4];
                         ldmatrix_x4_trans(vbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
-                        mma16816<T>::run(o[mt], a, pb0, pb1);
+                        mma16816<MT>::run(o[mt], a, pb0, pb1);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_bar[s]);
+                if (!F8 && lane == 0) mbar_arrive(&empty_bar[s]);
             }
             // hand this warp's state to the combiner
 #pragma unroll
@@ -758,14 +805,14 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
         } else {
             // ---------------------------------------------- FFMA consumer
-            constexpr int EPC = chunk16<T>::n;
+            constexpr int EPC = chunk16<MT>::n;
             constexpr int LPT = 32 / P;              // lanes per token
             constexpr int CPT = D / LPT;             // channels per lane for q.k
             constexpr int KCH = CPT / EPC;           // 16-byte chunks per lane for q.k
             constexpr int DPL = D / 32;              // channels per lane for p.v
             float *qs = ff_q + w * GMAX * D;
             float *ps = ff_p + w * GMAX * P;
-            for (int e = lane; e < G * D; e += 32) qs[e] = elem<T>::to_f(qb[e]);
+            for (int e = lane; e < G * D; e += 32) qs[e] = elem<MT>::to_f(qb[e]);
             __syncwarp();
             float o[GMAX][DPL], m[GMAX], l[GMAX];
 #pragma unroll
@@ -786,6 +833,20 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 const int nvalid = info[s].nvalid;
                 const unsigned char *kst = ring + (size_t)s * STAGE;
                 const unsigned char *vst = kst + TILE;
+                float zscale = p.scale_log2, vscale = 1.f;
+                if constexpr (F8) {
+                    if (nvalid > 0) {
+                        const float4 am = st_scale[s];
+                        zscale = p.scale_log2 * fp8_scale(am.x);
+                        vscale = fp8_scale(am.y);
+                        f8_to_half(kst, my_k, nvalid);
+                        f8_to_half(vst, my_v, nvalid);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty_bar[s]);   // the codes are copied out: free the stage
+                    kst = my_k;
+                    vst = my_v;
+                }
                 if (nvalid > 0) {
                     float acc[GMAX];
 #pragma unroll
@@ -794,7 +855,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     for (int x = 0; x < KCH; ++x) {
                         const int chunk = sl * KCH + x;
                         float f[EPC];
-                        chunk16<T>::unpack(*reinterpret_cast<const uint4 *>(kst + swz128_offset<P>(tk, chunk)), f);
+                        chunk16<MT>::unpack(*reinterpret_cast<const uint4 *>(kst + swz128_offset<P>(tk, chunk)), f);
 #pragma unroll
                         for (int gg = 0; gg < GMAX; ++gg)
 #pragma unroll
@@ -807,7 +868,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                         if (gg >= G) break;
                         float a = acc[gg];
                         if (LPT == 2) a += __shfl_xor_sync(0xffffffffu, a, 1);
-                        const float z = valid ? a * p.scale_log2 : -INFINITY;
+                        const float z = valid ? a * zscale : -INFINITY;
                         float mx = z;
 #pragma unroll
                         for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -821,15 +882,15 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                         m[gg] = nm;
 #pragma unroll
                         for (int x = 0; x < DPL; ++x) o[gg][x] *= al;
-                        if (sl == 0) ps[gg * P + tk] = pz;
+                        if (sl == 0) ps[gg * P + tk] = pz * vscale;   // FP8: V scale on the weight
                     }
                     __syncwarp();
                     for (int t = 0; t < nvalid; ++t) {
-                        const int byte = lane * DPL * ES;
+                        const int byte = lane * DPL * MES;
                         const unsigned char *vp = vst + swz128_offset<P>(t, byte >> 4) + (byte & 15);
                         float v[DPL];
 #pragma unroll
-                        for (int x = 0; x < DPL; ++x) v[x] = elem<T>::to_f(reinterpret_cast<const T *>(vp)[x]);
+                        for (int x = 0; x < DPL; ++x) v[x] = elem<MT>::to_f(reinterpret_cast<const MT *>(vp)[x]);
 #pragma unroll
                         for (int gg = 0; gg < GMAX; ++gg) {
                             if (gg >= G) break;
@@ -840,7 +901,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_bar[s]);
+                if (!F8 && lane == 0) mbar_arrive(&empty_bar[s]);
             }
             if (!wait_slot_free(kseg)) break;
 #pragma unroll
@@ -866,14 +927,15 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     // The single-launch kernel adds 4 selector warps; one consumer warp fewer
     // keeps its registers per thread at the two-kernel level.
     constexpr int NW = FUSED ? 7 : 8;
-    constexpr int STAGE = 2 * P * D * (int)sizeof(T);
+    constexpr bool F8 = is_fp8<T>::value;
+    constexpr int STAGE = 2 * P * D * (F8 ? 1 : (int)sizeof(T));
     AttnParams p = p0;
     // Pick the number of working consumer warps (up to NW-1) that allows the deepest ring
     // whose depth is a multiple of it (each stage owned by one consumer warp).
-    const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int);
+    const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int) + (F8 ? 16 : 0);
     int stages = 0, consumers = 0;
     for (int nw = NW - 1; nw >= 1; --nw) {   // the last consumer warp is the combiner
-        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages);
+        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);
         if (s > 32) s = 32;
@@ -886,7 +948,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     if (stages < 2) return cudaErrorInvalidConfiguration;
     p.stages = stages;
     p.consumers = consumers;
-    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B, FUSED, p.max_pages);
+    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8);
     auto kern = attn_kernel<T, D, P, MMA, GMAX, NW, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -913,7 +975,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
 template <typename T, int D, int P, bool FUSED>
 static cudaError_t launch_attn_dp(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p,
                                   int grid, size_t smem_budget, bool pdl, cudaStream_t stream) {
-    if constexpr (sizeof(T) == 2) {
+    if constexpr (is_fp8<T>::value || sizeof(T) == 2) {
         // tensor cores when the query group makes q.K a real contraction
         if (p.G >= 2) return launch_attn_t<T, D, P, true, 8, FUSED>(km, vm, p, grid, smem_budget, pdl, stream);
         return launch_attn_t<T, D, P, false, 1, FUSED>(km, vm, p, grid, smem_budget, pdl, stream);
@@ -937,6 +999,7 @@ cudaError_t launch_attention(qasa_dtype dt, int D, int P, const CUtensorMap &km,
                              const CUtensorMap &vm, const AttnParams &p, int grid,
                              size_t smem_budget, bool pdl, cudaStream_t stream) {
     switch (dt) {
+    case QASA_DTYPE_E4M3: return launch_attn_dt<fp8e4m3, false>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
     case QASA_DTYPE_F32: return launch_attn_dt<float, false>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
     case QASA_DTYPE_F16: return launch_attn_dt<__half, false>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
     default: return launch_attn_dt<__nv_bfloat16, false>(D, P, km, vm, p, grid, smem_budget, pdl, stream);
@@ -947,6 +1010,7 @@ cudaError_t launch_fused_decode(qasa_dtype dt, int D, int P, const CUtensorMap &
                                 const CUtensorMap &vm, const AttnParams &p, int grid,
                                 size_t smem_budget, cudaStream_t stream) {
     switch (dt) {
+    case QASA_DTYPE_E4M3: return cudaErrorNotSupported;   // the selection is not fused for FP8 KV
     case QASA_DTYPE_F32: return launch_attn_dt<float, true>(D, P, km, vm, p, grid, smem_budget, false, stream);
     case QASA_DTYPE_F16: return launch_attn_dt<__half, true>(D, P, km, vm, p, grid, smem_budget, false, stream);
     default: return launch_attn_dt<__nv_bfloat16, true>(D, P, km, vm, p, grid, smem_budget, false, stream);

@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -91,6 +92,38 @@ template <> struct chunk16<__nv_bfloat16> {
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
+
+// ------------------------------------------------------------- FP8 codes
+
+// Tag type of FP8 (E4M3) KV: the pools hold one-byte codes with a scale per
+// (page, KV head); queries, outputs and appended values are __half.
+struct fp8e4m3 {};
+template <typename T> struct is_fp8 { static constexpr bool value = false; };
+template <> struct is_fp8<fp8e4m3> { static constexpr bool value = true; };
+
+// Value of one E4M3 code (exact in fp32).
+__device__ __forceinline__ float e4m3_to_f(uint32_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+    return __half2float(__half(h));
+}
+// Nearest E4M3 code (ties to even, finite overflow saturates to +-448), with a
+// zero result stored as +0 so that equal values always have equal codes.
+__device__ __forceinline__ uint32_t e4m3_from_f(float x) {
+    const uint32_t c = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+    return (c & 0x7Fu) ? c : 0u;
+}
+// Two codes (low byte first) to a half2 word, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+// 16 codes (one 16-byte chunk) to 16 halves: channels 0..7 in lo, 8..15 in hi.
+__device__ __forceinline__ void e4m3x16_to_h(const uint4 &c, uint4 &lo, uint4 &hi) {
+    lo = make_uint4(e4m3x2_to_h2(c.x), e4m3x2_to_h2(c.x >> 16), e4m3x2_to_h2(c.y), e4m3x2_to_h2(c.y >> 16));
+    hi = make_uint4(e4m3x2_to_h2(c.z), e4m3x2_to_h2(c.z >> 16), e4m3x2_to_h2(c.w), e4m3x2_to_h2(c.w >> 16));
+}
+// Scale of a page from its amax (the fp32 division of the format).
+__device__ __forceinline__ float fp8_scale(float amax) { return __fdiv_rn(amax, 448.0f); }
 
 // ------------------------------------------------------------ shared rules
 

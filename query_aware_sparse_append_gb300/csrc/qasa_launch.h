@@ -21,6 +21,7 @@ struct AppendParams {
     const void *v_new;
     int32_t *status;
     int num_phys, Hkv, P, max_pages, T;
+    float *scales;       // FP8 KV: [num_phys][Hkv][4] (amax K, amax V, -, -)
 };
 
 struct SelectParams {
@@ -34,6 +35,7 @@ struct SelectParams {
     int32_t *counters;
     int32_t *status;
     int num_phys, Hkv, P, G, Hq, max_pages, max_budget;
+    const float *scales;   // FP8 KV: [num_phys][Hkv][4] (amax K, amax V, -, -)
 };
 
 struct AttnParams {
@@ -58,6 +60,7 @@ struct AttnParams {
     const void *bounds;
     float *scores_out;
     int32_t *ready;    // [units] 1 once a unit's kept ids are published (zero at launch)
+    const float *scales;   // FP8 KV: [num_phys][Hkv][4] (amax K, amax V, -, -)
 };
 
 struct MassParams {

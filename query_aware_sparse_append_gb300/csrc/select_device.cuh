@@ -285,6 +285,160 @@ __device__ void score_pages_mma_staged(const Grp &grp, const SelectParams &p, in
     }
 }
 
+// FP8 boxes (E4M3 codes, scale amax_K / 448 per page): tensor-core scores of the
+// codes, converted to halves exactly, times the page's scale (the common
+// factor of every box value of the page).  Lane c holds 16-byte code chunks
+// k = c + 4m of the [lo | hi] row, i.e. half chunks 2k and 2k+1, which feed MMA
+// slots 2m and 2m+1; the q fragments use the same channel order.
+template <int D, class Grp>
+__device__ void score_pages_fp8_mma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
+    constexpr int J = D / 16;          // MMA slots per lane per box row, as in the 16-bit path
+    constexpr int JC = J / 2;          // 16-byte code chunks per lane per box row
+    const int lane = grp.lane(), warp = grp.warp();
+    const int c = lane & 3, n = lane >> 2;
+
+    uint32_t qf[J][4];
+    const __half *qrow = static_cast<const __half *>(p.q) + ((size_t)b * p.Hq + (size_t)h * p.G + n) * D;
+#pragma unroll
+    for (int jj = 0; jj < J; ++jj) {
+        const int x = 2 * c + 8 * (jj >> 1) + (jj & 1);   // half chunk of the [lo | hi] row
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (n < p.G) raw = *reinterpret_cast<const uint4 *>(qrow + (x % (D / 8)) * 8);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t neg = ((w[i] & 0x80008000u) >> 15) * 0xffffu;
+            qf[jj][i] = (x < D / 8) ? (w[i] & neg) : (w[i] & ~neg);
+        }
+    }
+
+    const uint8_t *bounds = static_cast<const uint8_t *>(p.bounds);
+    const int32_t *bt = p.block_table + (size_t)b * p.max_pages;
+    const int ntiles = (N + 15) >> 4;
+    int nph0 = warp * 16 + n < N ? bt[warp * 16 + n] : -1;
+    int nph1 = warp * 16 + n + 8 < N ? bt[warp * 16 + n + 8] : -1;
+    for (int t = warp; t < ntiles; t += Grp::warps) {
+        const int r0 = t * 16 + n, r1 = r0 + 8;
+        const int ph0 = nph0, ph1 = nph1;
+        {
+            const int q0 = (t + Grp::warps) * 16 + n;
+            nph0 = q0 < N ? bt[q0] : -1;
+            nph1 = q0 + 8 < N ? bt[q0 + 8] : -1;
+        }
+        const bool ok0 = ph0 >= 0 && ph0 < p.num_phys, ok1 = ph1 >= 0 && ph1 < p.num_phys;
+        if (((r0 < N && !ok0) || (r1 < N && !ok1)) && p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
+        const size_t e0 = (size_t)(ok0 ? ph0 : 0) * p.Hkv + h, e1 = (size_t)(ok1 ? ph1 : 0) * p.Hkv + h;
+        const uint8_t *row0 = bounds + e0 * 2 * D;
+        const uint8_t *row1 = bounds + e1 * 2 * D;
+        const float am0 = ok0 ? p.scales[e0 * 4] : 0.f, am1 = ok1 ? p.scales[e1 * 4] : 0.f;
+        uint4 c0[JC], c1[JC];
+#pragma unroll
+        for (int m = 0; m < JC; ++m) {
+            c0[m] = ok0 ? ld_global_nc_v4(row0 + (c + 4 * m) * 16) : make_uint4(0, 0, 0, 0);
+            c1[m] = ok1 ? ld_global_nc_v4(row1 + (c + 4 * m) * 16) : make_uint4(0, 0, 0, 0);
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < JC; ++m) {
+            uint4 l0, h0, l1, h1;
+            e4m3x16_to_h(c0[m], l0, h0);
+            e4m3x16_to_h(c1[m], l1, h1);
+            {
+                const uint32_t fa[4] = {l0.x, l1.x, l0.y, l1.y};
+                mma16816<__half>::run(acc, fa, qf[2 * m][0], qf[2 * m][1]);
+                const uint32_t fb[4] = {l0.z, l1.z, l0.w, l1.w};
+                mma16816<__half>::run(acc, fb, qf[2 * m][2], qf[2 * m][3]);
+            }
+            {
+                const uint32_t fa[4] = {h0.x, h1.x, h0.y, h1.y};
+                mma16816<__half>::run(acc, fa, qf[2 * m + 1][0], qf[2 * m + 1][1]);
+                const uint32_t fb[4] = {h0.z, h1.z, h0.w, h1.w};
+                mma16816<__half>::run(acc, fb, qf[2 * m + 1][2], qf[2 * m + 1][3]);
+            }
+        }
+        const bool g0 = 2 * c < p.G, g1 = 2 * c + 1 < p.G;
+        float m0 = fmaxf(g0 ? acc[0] : -INFINITY, g1 ? acc[1] : -INFINITY);
+        float m1 = fmaxf(g0 ? acc[2] : -INFINITY, g1 ? acc[3] : -INFINITY);
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+        if (c == 0) {
+            if (r0 < N) sc[r0] = ok0 ? __fmul_rn(m0, fp8_scale(am0)) : -INFINITY;
+            if (r1 < N) sc[r1] = ok1 ? __fmul_rn(m1, fp8_scale(am1)) : -INFINITY;
+        }
+    }
+}
+
+// FP8 boxes, one query head per KV head (FFMA): lane groups of D/8 lanes hold
+// one box row (16 codes per lane); NB rows per round with all loads in flight.
+template <int D, int GMAX, class Grp>
+__device__ void score_pages_fp8_ffma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
+    constexpr int LPR = D / 8;                   // 2D codes per row / 16 per lane
+    constexpr int RPW = 32 / LPR;
+    constexpr int NB = 4;
+    const int lane = grp.lane(), warp = grp.warp();
+    const int rsub = lane / LPR, csub = lane % LPR;
+    const int G = p.G;
+    float qq[GMAX][16];
+    const __half *qb = static_cast<const __half *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+#pragma unroll
+    for (int g = 0; g < GMAX; ++g)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int idx = csub * 16 + e;
+            float v = 0.f;
+            if (g < G) {
+                const float qv = __half2float(qb[(size_t)g * D + (idx % D)]);
+                v = idx < D ? fminf(qv, 0.f) : fmaxf(qv, 0.f);
+            }
+            qq[g][e] = v;
+        }
+    const uint8_t *bounds = static_cast<const uint8_t *>(p.bounds);
+    const int32_t *bt = p.block_table + (size_t)b * p.max_pages;
+    const int npass = (N + RPW - 1) / RPW;
+    for (int pass0 = warp; pass0 < npass; pass0 += Grp::warps * NB) {
+        int page[NB];
+        bool ok[NB];
+        uint4 raw[NB];
+        float am[NB];
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            page[q] = (pass0 + q * Grp::warps) * RPW + rsub;
+            const bool in = pass0 + q * Grp::warps < npass && page[q] < N;
+            const int ph = in ? bt[page[q]] : -1;
+            ok[q] = ph >= 0 && ph < p.num_phys;
+            if (in && !ok[q] && csub == 0 && p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
+            const size_t e = (size_t)(ok[q] ? ph : 0) * p.Hkv + h;
+            raw[q] = ok[q] ? ld_global_nc_v4(bounds + e * 2 * D + csub * 16) : make_uint4(0, 0, 0, 0);
+            am[q] = ok[q] ? p.scales[e * 4] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            if (pass0 + q * Grp::warps >= npass) break;      // warp-uniform
+            const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+            float acc[GMAX];
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) acc[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float f = e4m3_to_f((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
+#pragma unroll
+                for (int g = 0; g < GMAX; ++g) acc[g] = fmaf(qq[g][e], f, acc[g]);
+            }
+            float best = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+                float a = acc[g];
+#pragma unroll
+                for (int off = 1; off < LPR; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+                if (g < G) best = fmaxf(best, a);
+            }
+            if (csub == 0 && page[q] < N) sc[page[q]] = ok[q] ? __fmul_rn(best, fp8_scale(am[q])) : -INFINITY;
+        }
+    }
+}
+
 // FFMA scores (any dtype, G <= GMAX).
 template <typename T, int D, int GMAX, class Grp>
 __device__ void score_pages_ffma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
@@ -388,7 +542,10 @@ __device__ void select_unit(const Grp &grp, const SelectParams &p, int u, float 
     }
     const bool need_scores = (k < N) || (p.scores_out != nullptr);
     if (need_scores) {
-        if constexpr (MMA) {
+        if constexpr (is_fp8<T>::value) {
+            if constexpr (MMA) score_pages_fp8_mma<D>(grp, p, b, h, N, sc);
+            else score_pages_fp8_ffma<D, GMAX>(grp, p, b, h, N, sc);
+        } else if constexpr (MMA) {
             if (stage) score_pages_mma_staged<T, D>(grp, p, b, h, N, sc, *stage, *phase_bits);
             else score_pages_mma<T, D>(grp, p, b, h, N, sc);
         } else {

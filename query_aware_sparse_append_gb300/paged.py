@@ -15,12 +15,15 @@ import torch
 
 from . import workloads as W
 
-TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+               "e4m3": torch.float16}          # the dtype of q, out and appended K/V
+POOL_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+              "e4m3": torch.uint8}             # the dtype of the pools and boxes
 
 
 def to_torch(x: np.ndarray, dtype: str) -> torch.Tensor:
     """Host tensor sharing the bits of a storage-dtype numpy array."""
-    if dtype == "bf16":
+    if W.input_dtype(dtype) == "bf16":
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
     return torch.from_numpy(np.ascontiguousarray(x))
 
@@ -73,11 +76,14 @@ def load(wl: DeviceWorkload, device="cuda", poison: bool = False,
     cfg = wl.cfg
     dev = torch.device(device)
     cache = qasa.PagedKVCache.empty(wl.plan.num_phys_pages, cfg.num_kv_heads, cfg.page_size,
-                                    cfg.head_dim, TORCH_DTYPE[cfg.dtype], dev)
+                                    cfg.head_dim, POOL_DTYPE[cfg.dtype], dev)
     if poison:
-        cache.k_pool.fill_(float("nan"))
-        cache.v_pool.fill_(float("nan"))
-        cache.page_bounds.fill_(float("nan"))
+        nan = 0x7F if cfg.dtype == "e4m3" else float("nan")   # E4M3 NaN code
+        cache.k_pool.fill_(nan)
+        cache.v_pool.fill_(nan)
+        cache.page_bounds.fill_(nan)
+        if cache.page_scales is not None:
+            cache.page_scales.fill_(float("nan"))
     bt = torch.from_numpy(wl.plan.block_table).to(dev)
     B = cfg.batch
     lens = wl.lens.astype(np.int64)

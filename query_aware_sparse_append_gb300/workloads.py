@@ -17,7 +17,8 @@ regenerated alone (the oracle re-derives single sequences at full size).
 
 Storage dtypes: ``"f32"`` -> numpy float32, ``"f16"`` -> numpy float16,
 ``"bf16"`` -> numpy uint16 holding bfloat16 bit patterns (round-to-nearest-even
-from float32, done by torch's CPU cast).
+from float32, done by torch's CPU cast).  ``"e4m3"`` (FP8 KV cache) draws its
+queries and the K/V values it appends as float16: the cache quantizes them.
 """
 from __future__ import annotations
 
@@ -27,7 +28,12 @@ from typing import List, Optional, Sequence
 
 import numpy as np
 
-DTYPES = ("f32", "f16", "bf16")
+DTYPES = ("f32", "f16", "bf16", "e4m3")
+
+
+def input_dtype(dtype: str) -> str:
+    """Dtype of the queries and of the appended K/V values of a workload."""
+    return "f16" if dtype == "e4m3" else dtype
 
 # stream ids inside a SeedSequence
 _S_SEQ = 0          # per-sequence q, K, V
@@ -97,6 +103,10 @@ CONFIGS = {
     "headline_8k": Workload("headline_8k", 6, batch=128, num_q_heads=32, num_kv_heads=4,
                             head_dim=128, page_size=16, dtype="f16", ctx_min=8192,
                             ctx_max=8192, budget_kind="permille", budget_value=125),
+    # the headline shapes with an FP8 (E4M3) KV cache
+    "headline_8k_e4m3": Workload("headline_8k_e4m3", 7, batch=128, num_q_heads=32, num_kv_heads=4,
+                                 head_dim=128, page_size=16, dtype="e4m3", ctx_min=8192,
+                                 ctx_max=8192, budget_kind="permille", budget_value=125),
 }
 
 SERVING_MIX_BUDGETS_PERMILLE = (50, 125, 250, 500, 1000)
@@ -110,6 +120,7 @@ def _rng(seed: int, cfg: Workload, stream: int, index: int = 0) -> np.random.Gen
 def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
     """Cast float32 samples to the storage dtype (bf16 as uint16 bit patterns)."""
     x = np.asarray(x, dtype=np.float32)
+    dtype = input_dtype(dtype)
     if dtype == "f32":
         return x
     if dtype == "f16":
@@ -123,6 +134,7 @@ def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
 
 def widen(x: np.ndarray, dtype: str) -> np.ndarray:
     """Exact float64 values of stored elements."""
+    dtype = input_dtype(dtype)
     if dtype == "bf16":
         u = np.asarray(x, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
         return u.view(np.float32).astype(np.float64)
@@ -130,7 +142,7 @@ def widen(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def np_storage_dtype(dtype: str):
-    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}[dtype]
+    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}[input_dtype(dtype)]
 
 
 def seq_lens(cfg: Workload, seed: int = 0) -> np.ndarray:

@@ -75,6 +75,32 @@ def make_case(cfg: W.Workload, seed: int = 0, batch: Optional[int] = None, lens=
     return case
 
 
+def chunk_lens(L: int, append_chunks: Optional[List[int]]) -> List[int]:
+    """The append sizes paged.load uses for a sequence of L tokens."""
+    out, done = [], 0
+    for c in (append_chunks or [L]):
+        t = min(L - done, c)
+        if t > 0:
+            out.append(t)
+            done += t
+    return out
+
+
+def fp8_unit(case: Case, b: int, h: int, append_chunks: Optional[List[int]] = None):
+    """The oracle's FP8 cache of one (sequence, KV head), replaying the appends:
+    codes, amax and boxes of K and V, and the exact dequantized values."""
+    P = case.cfg.page_size
+    L = int(case.lens[b])
+    ch = chunk_lens(L, append_chunks)
+    kc, ka, lo, hi = oracle.fp8_append_replay(case.k64(b, h).astype(np.float32), P, ch)
+    vc, va, _, _ = oracle.fp8_append_replay(case.v64(b, h).astype(np.float32), P, ch)
+    sk, sv = oracle.fp8_scale(ka), oracle.fp8_scale(va)
+    tok_page = np.arange(L) // P
+    return dict(k_codes=kc, k_amax=ka, lo=lo, hi=hi, v_codes=vc, v_amax=va,
+                K=oracle.fp8_dequant(kc, sk[tok_page]), V=oracle.fp8_dequant(vc, sv[tok_page]),
+                LO=oracle.fp8_dequant(lo, sk), HI=oracle.fp8_dequant(hi, sk))
+
+
 def build_device(case: Case, append_chunks=None, poison=True):
     return paged.load(case, poison=poison, append_chunks=append_chunks)
 
