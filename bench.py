@@ -33,7 +33,7 @@ METRIC = "sparse decode queries/sec and HBM GB/s (% roofline) at 8K ctx, 12.5% b
 L2_FLUSH_BYTES = 256 << 20        # written between timed steps (evicts the step's data)
 L2_CLEAN_BYTES = 512 << 20        # then read, so the flush's dirty lines are written back
                                   # before the next timed step instead of during it
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attention_headline_8k.md")
+PROFILE_DIR = os.path.join(ROOT, "profiles")   # attention_<workload>.md: ncu summary of the attention kernel
 
 
 # ------------------------------------------------------------ distributed
@@ -71,16 +71,21 @@ def barrier(device=None):
 
 def algorithmic_bytes(cfg, lens, budgets):
     """Bytes the method must move per step (and per kernel), per (sequence, KV head):
-    select:    N_b*2*d*es (page boxes) + G*d*es (q) + 4*N_b (block table) + 4*k_b (ids out)
-    attention: k_b*2*P*d*es (kept K and V page tiles) + 2*G*d*es (q, out) + 8*k_b (ids, table)
+    select:    N_b*2*d*es (page boxes) + G*d*qs (q) + 4*N_b (block table) + 4*k_b (ids out)
+    attention: k_b*2*P*d*es (kept K and V page tiles) + 2*G*d*qs (q, out) + 8*k_b (ids, table)
+    es = bytes per stored KV element, qs = bytes per query / output element.
+    FP8 KV adds the page scales: 4*N_b (K amax) to the selection, 16*k_b (one
+    16-byte scale record per kept page) to the attention.
     """
-    es = 4 if cfg.dtype == "f32" else 2
+    es = {"f32": 4, "e4m3": 1}.get(cfg.dtype, 2)
+    qs = 4 if cfg.dtype == "f32" else 2
     d, P, G, Hkv = cfg.head_dim, cfg.page_size, cfg.group, cfg.num_kv_heads
     N = (np.asarray(lens, np.int64) + P - 1) // P
     k = np.minimum(N, np.maximum(np.asarray(budgets, np.int64), np.minimum(N, 2)))
-    sel = Hkv * (N * 2 * d * es + G * d * es + 4 * N + 4 * k)
-    att = Hkv * (k * 2 * P * d * es + 2 * G * d * es + 8 * k)
-    dense = Hkv * (N * 2 * P * d * es + 2 * G * d * es + 4 * N)
+    f8 = cfg.dtype == "e4m3"
+    sel = Hkv * (N * 2 * d * es + G * d * qs + 4 * N + 4 * k + (4 * N if f8 else 0))
+    att = Hkv * (k * 2 * P * d * es + 2 * G * d * qs + 8 * k + (16 * k if f8 else 0))
+    dense = Hkv * (N * 2 * P * d * es + 2 * G * d * qs + 4 * N + (16 * N if f8 else 0))
     return int(sel.sum()), int(att.sum()), int(dense.sum())
 
 
@@ -88,7 +93,7 @@ def rebuild_bytes(cfg, lens):
     """Algorithmic bytes of rebuilding every page box: the valid keys read once,
     the boxes written once, the block-table entries read."""
     import numpy as np
-    es = 4 if cfg.dtype == "f32" else 2
+    es = {"f32": 4, "e4m3": 1}.get(cfg.dtype, 2)
     lens = np.asarray(lens, dtype=np.int64)
     n = (lens + cfg.page_size - 1) // cfg.page_size
     return int(cfg.num_kv_heads * cfg.head_dim * es * (lens.sum() + 2 * n.sum()) + 4 * n.sum())
@@ -127,11 +132,11 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(workload="headline_8k"):
     """DRAM bytes per attention launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+    taken on the current kernel source and on this workload (else None)."""
     try:
-        with open(PROFILE_SUMMARY) as f:
+        with open(os.path.join(PROFILE_DIR, "attention_%s.md" % workload)) as f:
             text = f.read()
     except OSError:
         return None
@@ -141,6 +146,8 @@ def profiled_traffic():
             k, _, v = line[len("bench-key "):].partition("=")
             vals[k.strip()] = v.strip()
     if vals.get("source_digest") != kernel_source_digest():
+        return None
+    if vals.get("workload", "headline_8k") != workload:
         return None
     try:
         return int(vals["dram_bytes_per_launch_full_size"])
@@ -305,7 +312,16 @@ def oracle_sample(cfg, seed, seconds=15.0, threads=None):
             K = W.widen(s.k[:, h], cfg.dtype)
             V = W.widen(s.v[:, h], cfg.dtype)
             q = W.widen(s.q[h * G:(h + 1) * G], cfg.dtype)
-            lo, hi = oracle.page_bounds(K, P)
+            if cfg.dtype == "e4m3":      # the cache's codes and scales, as one append writes them
+                L = int(lens[b])
+                tok = np.arange(L) // P
+                kc, ka, klo, khi = oracle.fp8_append_replay(K.astype(np.float32), P, [L])
+                vc, va, _, _ = oracle.fp8_append_replay(V.astype(np.float32), P, [L])
+                sk, sv = oracle.fp8_scale(ka), oracle.fp8_scale(va)
+                K, V = oracle.fp8_dequant(kc, sk[tok]), oracle.fp8_dequant(vc, sv[tok])
+                lo, hi = oracle.fp8_dequant(klo, sk), oracle.fp8_dequant(khi, sk)
+            else:
+                lo, hi = oracle.page_bounds(K, P)
             units.append((q, K, V, lo, hi, int(lens[b]), int(bud[b])))
         b += 1
 
@@ -351,7 +367,8 @@ def run_reference(args):
     return 0
 
 
-def config_block(cfg):
+def config_block(cfg, step_bytes=None):
+    mb = "%.0f MB" % (step_bytes / 1e6) if step_bytes else "the step's bytes"
     return {"workload": cfg.name, "batch": cfg.batch, "ctx": [cfg.ctx_min, cfg.ctx_max],
             "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
             "head_dim": cfg.head_dim, "page_size": cfg.page_size,
@@ -359,7 +376,7 @@ def config_block(cfg):
                        if cfg.budget_kind == "permille" else "%d pages" % cfg.budget_value),
             "kv_dtype": cfg.dtype, "physical_pages": "shuffled",
             "l2": "between timed steps a 256 MB write evicts L2, then a 512 MB read leaves it "
-                  "clean; per-step bytes (407 MB) also exceed L2"}
+                  "clean; per-step bytes (%s) also exceed L2" % mb}
 
 
 # ------------------------------------------------------------ GPU leg
@@ -553,7 +570,8 @@ def run_ours(args):
     dense_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in evd)
 
     # ---- page hit rate of the selection against the dense attention mass
-    hit = hit_rate_stats(qasa, wl, wl.budget_dev, wl.budgets, max_budget, sel)
+    # (measured on 16/32-bit caches only)
+    hit = hit_rate_stats(qasa, wl, wl.budget_dev, wl.budgets, max_budget, sel) if cfg.dtype != "e4m3" else None
 
     # ---- bulk rebuild of every page box from the pool (same boxes written back)
     evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
@@ -615,10 +633,10 @@ def run_ours(args):
         "ms_per_step": ms_all,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic",
-        "config": config_block(cfg),
+        "config": config_block(cfg, sel_b + att_b),
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (sparse attention over kept pages)",
                      "achieved": att_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": att_gbs / peak, "traffic": profiled_traffic(),
+                     "frac": att_gbs / peak, "traffic": profiled_traffic(cfg.name),
                      "algorithmic_bytes_per_launch": att_b, "ms_per_launch": att_ms,
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
