@@ -312,6 +312,32 @@ qasa_status qasa_page_hit_rate(const qasa_kv_cache *cache, const float *mass, in
                                int32_t *hits, float *covered_mass, float *best_mass,
                                int32_t *device_status, cudaStream_t stream);
 
+/*
+ * The decode step with its per-call inputs and outputs in HOST memory (the
+ * KV cache stays on the device): enqueues on `stream` one cudaMemcpyAsync per
+ * input (q, block table, seq_lens, budget_pages) into `workspace`, the step of
+ * qasa_sparse_decode_attention, and one copy per output (out, selected) back.
+ * The paper has no counterpart; this is the call a host-driven server makes.
+ *   q_host, out_host            [batch][num_q_heads][head_dim] (f16 for FP8 KV)
+ *   block_table_host            [batch][max_pages_per_seq] int32
+ *   seq_lens_host, budget_pages_host  [batch] int32
+ *   selected_host               [batch][num_kv_heads][max_budget] int32
+ *   workspace                   device memory of qasa_host_decode_workspace_size
+ *                               bytes, 256-byte aligned (scratch, no initialisation)
+ * The outputs are valid once the stream has been synchronised.  Host buffers
+ * should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to be
+ * asynchronous.  Errors as in qasa_sparse_decode_attention.
+ */
+size_t qasa_host_decode_workspace_size(int32_t batch, int32_t num_q_heads, const qasa_kv_cache *cache,
+                                       int32_t max_pages_per_seq, int32_t max_budget);
+qasa_status qasa_sparse_decode_attention_host(const qasa_kv_cache *cache, const void *q_host,
+                                              int32_t num_q_heads, const int32_t *block_table_host,
+                                              int32_t max_pages_per_seq, const int32_t *seq_lens_host,
+                                              const int32_t *budget_pages_host, int32_t max_budget,
+                                              float scale, void *out_host, int32_t *selected_host,
+                                              void *workspace, size_t workspace_bytes, int32_t batch,
+                                              int32_t *device_status, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char *qasa_status_string(qasa_status status);
 

@@ -69,6 +69,11 @@ _lib.qasa_page_attention_mass.argtypes = [_C, _P, _I, _P, _I, _P, ctypes.c_float
 _lib.qasa_page_attention_mass.restype = _I
 _lib.qasa_page_hit_rate.argtypes = [_C, _P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P]
 _lib.qasa_page_hit_rate.restype = _I
+_lib.qasa_host_decode_workspace_size.argtypes = [_I, _I, _C, _I, _I]
+_lib.qasa_host_decode_workspace_size.restype = ctypes.c_size_t
+_lib.qasa_sparse_decode_attention_host.argtypes = [_C, _P, _I, _P, _I, _P, _P, _I, ctypes.c_float, _P, _P, _P,
+                                                   ctypes.c_size_t, _I, _P, _P]
+_lib.qasa_sparse_decode_attention_host.restype = _I
 _lib.qasa_status_string.argtypes = [_I]
 _lib.qasa_status_string.restype = ctypes.c_char_p
 _lib.qasa_version.restype = _I
@@ -77,6 +82,7 @@ EXPORTED = ("qasa_kv_append", "qasa_decode_workspace_size", "qasa_select_pages",
             "qasa_sparse_attention", "qasa_sparse_decode_attention",
             "qasa_dense_decode_attention", "qasa_sparse_decode_attention_noalloc",
             "qasa_rebuild_page_bounds", "qasa_page_attention_mass", "qasa_page_hit_rate",
+            "qasa_host_decode_workspace_size", "qasa_sparse_decode_attention_host",
             "qasa_status_string", "qasa_version")
 
 
@@ -304,6 +310,34 @@ def sparse_decode_attention_noalloc(cache: PagedKVCache, q: torch.Tensor, block_
         cache.c_ref, _ptr(_contig(q, "q")), Hq, _ptr(block_table), int(block_table.shape[1]),
         _ptr(seq_lens), _ptr(bud), int(max_budget), float(scale or 0.0), _ptr(out), _ptr(selected),
         _ptr(scores), B, _ptr(status), _stream(stream)))
+
+
+def alloc_host_workspace(cache: PagedKVCache, batch: int, num_q_heads: int, max_pages_per_seq: int,
+                         max_budget: int, device=None) -> torch.Tensor:
+    n = int(_lib.qasa_host_decode_workspace_size(batch, num_q_heads, cache.c_ref, max_pages_per_seq, max_budget))
+    if batch and not n:
+        raise QasaError("unsupported shape for the host-buffer decode step")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or cache.k_pool.device)
+
+
+def sparse_decode_attention_host(cache: PagedKVCache, q_host: torch.Tensor, block_table_host: torch.Tensor,
+                                 seq_lens_host: torch.Tensor, budget_host: torch.Tensor, max_budget: int,
+                                 out_host: torch.Tensor, selected_host: torch.Tensor,
+                                 workspace: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                                 status: Optional[torch.Tensor] = None, stream=None) -> int:
+    """The decode step with host (preferably pinned) inputs and outputs; the
+    copies and kernels are enqueued on the stream (synchronise before reading)."""
+    B, Hq = int(q_host.shape[0]), int(q_host.shape[1])
+    maxp = int(block_table_host.shape[1])
+    if workspace is None:
+        workspace = alloc_host_workspace(cache, B, Hq, maxp, max_budget)
+    code = _lib.qasa_sparse_decode_attention_host(
+        cache.c_ref, _ptr(_contig(q_host, "q_host")), Hq, _ptr(_contig(block_table_host, "block_table_host")), maxp,
+        _ptr(_contig(seq_lens_host, "seq_lens_host")), _ptr(_contig(budget_host, "budget_host")), int(max_budget),
+        float(scale or 0.0), _ptr(_contig(out_host, "out_host")), _ptr(_contig(selected_host, "selected_host")),
+        _ptr(workspace), workspace.numel(), B, _ptr(status), _stream(stream))
+    _check(code, "qasa_sparse_decode_attention_host")
+    return code
 
 
 def dense_decode_attention(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,

@@ -3,6 +3,7 @@
 // include/qasa.h together with its contract.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <mutex>
@@ -55,19 +56,26 @@ qasa_status check_decode(const qasa_kv_cache *c, const void *q, int num_q_heads,
     return QASA_OK;
 }
 
-int sm_count() {
+// Per-device attributes, queried once per device (they cannot change).
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_optin[kMaxDevices];
+
+int device_attr(std::atomic<int> *cache, cudaDeviceAttr attr) {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    if (cudaDeviceGetAttribute(&n, attr, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
-size_t smem_optin() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-    return (size_t)n;
-}
+int sm_count() { return device_attr(g_sm_count, cudaDevAttrMultiProcessorCount); }
+
+size_t smem_optin() { return (size_t)device_attr(g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin); }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -135,13 +143,16 @@ qasa_status pool_tensor_map(CUtensorMap *map, void *base, const qasa_kv_cache *c
                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint64_t rows = (cuuint64_t)c->num_phys_pages * c->num_kv_heads * c->page_size;
     if (c->dtype == QASA_DTYPE_E4M3) {
-        // FP8 codes: one unswizzled box of head_dim bytes x page_size rows per tile
+        // FP8 codes: one box of head_dim bytes x page_size rows per tile; 128-byte
+        // swizzle at head_dim 128 (the tensor-core path reads it with ldmatrix),
+        // none at 64 (converted with plain row reads)
         cuuint64_t dims[2] = {(cuuint64_t)c->head_dim, rows};
         cuuint64_t strides[1] = {(cuuint64_t)c->head_dim};
         cuuint32_t box[2] = {(cuuint32_t)c->head_dim, (cuuint32_t)c->page_size};
         cuuint32_t estr[2] = {1, 1};
         CUresult r8 = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          c->head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         return r8 == CUDA_SUCCESS ? QASA_OK : QASA_ERR_DRIVER;
     }

@@ -36,6 +36,7 @@
 //
 // Every wait is bounded: a wait that gives up sets QASA_DEVERR_TIMEOUT, the CTA
 // stops issuing, drains the copies it issued (again bounded) and returns.
+#include <cstdlib>
 #include <type_traits>
 
 #include "select_device.cuh"
@@ -55,13 +56,13 @@ constexpr int kSelStageSlots = 4 * kSelSlotsPerWarp;
 
 // Host-side size of the dynamic shared memory (mirrors the device carve-up).
 size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int P, bool mma, int B,
-                       bool fused, int max_pages, bool fp8 = false) {
+                       bool fused, int max_pages, bool fp8 = false, bool fp8_scratch = false) {
     size_t s = 1024;                                   // alignment slack for the ring
     s += (size_t)stages * stage_bytes;
     s += (size_t)stages * 2 * sizeof(uint64_t);        // full / empty barriers
     s += (size_t)stages * (sizeof(StageInfo) + sizeof(int));
     if (fp8) s += 16 + (size_t)stages * 16;            // per-stage page scales
-    if (fp8) s += 1024 + (size_t)nw * 2 * P * D * 2;   // per-warp half copies of the K and V tiles
+    if (fp8_scratch) s += 1024 + (size_t)nw * 2 * P * D * 2;   // per-warp half copies of the K and V tiles
     s += (size_t)nw * gmax * (D + 2) * sizeof(float);  // combine scratch
     if (!mma) s += (size_t)nw * gmax * (D + P) * sizeof(float);
     s += (size_t)(2 * B + 2) * sizeof(int);            // prefix, lengths
@@ -103,6 +104,11 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     using MT = typename std::conditional<F8, __half, T>::type;   // q, out and MMA operand type
     constexpr int ES = F8 ? 1 : (int)sizeof(T);  // bytes per stored KV element
     constexpr int MES = (int)sizeof(MT);         // bytes per element of the tiles the consumers read
+    // FP8, d = 128, G >= 2: q.K on FP8 tensor cores straight from the (128-byte
+    // swizzled) code tiles, P.V from V fragments converted in registers;
+    // otherwise FP8 tiles are converted to half copies in shared memory
+    constexpr bool F8MMA = F8 && MMA && D == 128;
+    constexpr bool F8CONV = F8 && !F8MMA;
     constexpr int TILE = P * D * ES;            // one (page, head) tile of K or V
     constexpr int STAGE = 2 * TILE;
     constexpr int NSUB = F8 ? 1 : D * ES / 128; // 128-byte column boxes per tile
@@ -678,14 +684,69 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
 
         if constexpr (MMA) {
             const int cq = lane & 3, nq = lane >> 2;
-            uint32_t qf[D / 16][2];
+            uint32_t qf[F8MMA ? 1 : D / 16][2];
+            // FP8: q of head nq, scaled by 2^e (largest |q| in [128, 256)), split
+            // exactly into three E4M3 terms q * 2^e = t1 + t2/16 + t3/256; the B
+            // fragments hold channels 32kk + 4cq.. (b0) and 32kk + 16 + 4cq.. (b1)
+            uint32_t q8[F8MMA ? 3 : 1][F8MMA ? D / 32 : 1][2];
+            float ie0 = 1.f, ie1 = 1.f;                  // 2^-e of heads 2cq and 2cq + 1
+            if constexpr (F8MMA) {
+                float qv[D / 32][8];
+                float amax = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                qf[ks][0] = 0u; qf[ks][1] = 0u;
-                if (nq < G) {
-                    const MT *qr = qb + (size_t)nq * D + ks * 16 + 2 * cq;
-                    qf[ks][0] = *reinterpret_cast<const uint32_t *>(qr);
-                    qf[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    uint2 r0 = make_uint2(0, 0), r1 = make_uint2(0, 0);
+                    if (nq < G) {
+                        const MT *qr = qb + (size_t)nq * D + kk * 32 + 4 * cq;
+                        r0 = *reinterpret_cast<const uint2 *>(qr);
+                        r1 = *reinterpret_cast<const uint2 *>(qr + 16);
+                    }
+                    const uint32_t wq[4] = {r0.x, r0.y, r1.x, r1.y};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wq[x]));
+                        qv[kk][2 * x] = f.x;
+                        qv[kk][2 * x + 1] = f.y;
+                        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int e = amax > 0.f ? 7 - ilogbf(amax) : 0;
+                const float up = ldexpf(1.f, e);
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    uint32_t t[3][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}};
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const float v = qv[kk][x] * up;                 // exact
+                        const uint32_t c1 = e4m3_from_f(v);
+                        const float r1 = (v - e4m3_to_f(c1)) * 16.f;    // exact
+                        const uint32_t c2 = e4m3_from_f(r1);
+                        const float r2 = (r1 - e4m3_to_f(c2)) * 16.f;
+                        const uint32_t c3 = e4m3_from_f(r2);
+                        t[0][x >> 2] |= c1 << (8 * (x & 3));
+                        t[1][x >> 2] |= c2 << (8 * (x & 3));
+                        t[2][x >> 2] |= c3 << (8 * (x & 3));
+                    }
+#pragma unroll
+                    for (int tt = 0; tt < 3; ++tt) {
+                        q8[tt][kk][0] = t[tt][0];
+                        q8[tt][kk][1] = t[tt][1];
+                    }
+                }
+                const float down = ldexpf(1.f, -e);
+                ie0 = __shfl_sync(0xffffffffu, down, 8 * cq);        // head 2cq: lanes 4*(2cq)..
+                ie1 = __shfl_sync(0xffffffffu, down, 8 * cq + 4);
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    qf[ks][0] = 0u; qf[ks][1] = 0u;
+                    if (nq < G) {
+                        const MT *qr = qb + (size_t)nq * D + ks * 16 + 2 * cq;
+                        qf[ks][0] = *reinterpret_cast<const uint32_t *>(qr);
+                        qf[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+                    }
                 }
             }
             float o[D / 16][4];
@@ -706,7 +767,14 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 unsigned char *vst = kst + TILE;
                 uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
                 float zscale = p.scale_log2, vscale = 1.f;
-                if constexpr (F8) {
+                if constexpr (F8MMA) {
+                    if (nvalid > 0) {
+                        const float4 am = st_scale[s];
+                        zscale = p.scale_log2 * fp8_scale(am.x);
+                        vscale = fp8_scale(am.y);
+                    }
+                }
+                if constexpr (F8CONV) {
                     if (nvalid > 0) {
                         const float4 am = st_scale[s];
                         zscale = p.scale_log2 * fp8_scale(am.x);
@@ -732,14 +800,34 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 for (int sub = 0; sub < P / 16; ++sub) {
                     if (sub * 16 >= nvalid) break;
                     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (F8MMA) {
+                        // S^T = K q^T on FP8 tensor cores: the code tile rows feed the
+                        // A fragments as they are; one accumulator per q term
+                        float s3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const int tok = sub * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                        const int chn = 2 * ks + (lane >> 4);
-                        uint32_t a[4];
-                        ldmatrix_x4(kbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
-                        if (ks & 1) mma16816<MT>::run(sb, a, qf[ks][0], qf[ks][1]);
-                        else mma16816<MT>::run(sa, a, qf[ks][0], qf[ks][1]);
+                        for (int kk = 0; kk < D / 32; ++kk) {
+                            const int tok = sub * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                            uint32_t a[4];
+                            ldmatrix_x4(kbase + swz128_offset<P>(tok, 2 * kk + (lane >> 4)), a[0], a[1], a[2], a[3]);
+                            mma_e4m3_16832(sa, a, q8[0][kk][0], q8[0][kk][1]);
+                            mma_e4m3_16832(sb, a, q8[1][kk][0], q8[1][kk][1]);
+                            mma_e4m3_16832(s3, a, q8[2][kk][0], q8[2][kk][1]);
+                        }
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            sa[x] = (sa[x] + sb[x] * 0.0625f + s3[x] * 0.00390625f) * ((x & 1) ? ie1 : ie0);
+                            sb[x] = 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const int tok = sub * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                            const int chn = 2 * ks + (lane >> 4);
+                            uint32_t a[4];
+                            ldmatrix_x4(kbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
+                            if (ks & 1) mma16816<MT>::run(sb, a, qf[ks][0], qf[ks][1]);
+                            else mma16816<MT>::run(sa, a, qf[ks][0], qf[ks][1]);
+                        }
                     }
                     const int t0 = sub * 16 + (lane >> 2), t1 = t0 + 8;
                     const bool v0 = t0 < nvalid, v1 = t1 < nvalid;
@@ -760,24 +848,48 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     l0 = l0 * al0 + p0 + p2;
                     l1 = l1 * al1 + p1 + p3;
                     m0 = n0; m1 = n1;
+                    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {   // the maximum moved
 #pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+                        }
                     }
                     // FP8: the page's V scale rides on the weights (l keeps the plain sum)
                     const uint32_t pb0 = movmatrix_trans(mma16816<MT>::pack2(p0 * vscale, p1 * vscale));
                     const uint32_t pb1 = movmatrix_trans(mma16816<MT>::pack2(p2 * vscale, p3 * vscale));
+                    if constexpr (F8MMA) {
+                        // V^T fragments from the code tile: ldmatrix.trans hands a lane
+                        // the codes of tokens (2cq, 2cq+1) x channels (2nq, 2nq+1) of a
+                        // 16-channel chunk; byte permutes regroup them per channel and
+                        // each pair converts to halves.  Row nq of M-tile j is channel
+                        // 16j + 2nq, row nq + 8 is channel 16j + 2nq + 1.
 #pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        const int tok = sub * 16 + (lane & 7) + (lane >> 4) * 8;
-                        const int chn = 2 * mt + ((lane >> 3) & 1);
-                        uint32_t a[4];
-                        ldmatrix_x4_trans(vbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
-                        mma16816<MT>::run(o[mt], a, pb0, pb1);
+                        for (int j = 0; j < D / 16; j += 2) {
+                            const int tok = sub * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                            uint32_t r[4];
+                            ldmatrix_x4_trans(vbase + swz128_offset<P>(tok, j + (lane >> 4)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const uint32_t X = __byte_perm(r[2 * hf], r[2 * hf + 1], 0x6420);
+                                const uint32_t Y = __byte_perm(r[2 * hf], r[2 * hf + 1], 0x7531);
+                                const uint32_t a[4] = {e4m3x2_to_h2(X), e4m3x2_to_h2(Y), e4m3x2_to_h2(X >> 16),
+                                                       e4m3x2_to_h2(Y >> 16)};
+                                mma16816<MT>::run(o[j + hf], a, pb0, pb1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            const int tok = sub * 16 + (lane & 7) + (lane >> 4) * 8;
+                            const int chn = 2 * mt + ((lane >> 3) & 1);
+                            uint32_t a[4];
+                            ldmatrix_x4_trans(vbase + swz128_offset<P>(tok, chn), a[0], a[1], a[2], a[3]);
+                            mma16816<MT>::run(o[mt], a, pb0, pb1);
+                        }
                     }
                 }
                 __syncwarp();
-                if (!F8 && lane == 0) mbar_arrive(&empty_bar[s]);
+                if (!F8CONV && lane == 0) mbar_arrive(&empty_bar[s]);
             }
             // hand this warp's state to the combiner
 #pragma unroll
@@ -789,14 +901,17 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             const int h0 = 2 * cq, h1 = 2 * cq + 1;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-                const int ch = mt * 16 + nq;
+                // accumulator rows nq / nq + 8 of M-tile mt: channels mt*16 + nq / + 8
+                // (FP8 tensor-core path: mt*16 + 2nq / + 1)
+                const int ch = F8MMA ? mt * 16 + 2 * nq : mt * 16 + nq;
+                const int ch2 = F8MMA ? ch + 1 : ch + 8;
                 if (h0 < G) {
                     scr_o[(w * GMAX + h0) * D + ch] = o[mt][0];
-                    scr_o[(w * GMAX + h0) * D + ch + 8] = o[mt][2];
+                    scr_o[(w * GMAX + h0) * D + ch2] = o[mt][2];
                 }
                 if (h1 < G) {
                     scr_o[(w * GMAX + h1) * D + ch] = o[mt][1];
-                    scr_o[(w * GMAX + h1) * D + ch + 8] = o[mt][3];
+                    scr_o[(w * GMAX + h1) * D + ch2] = o[mt][3];
                 }
             }
             if (nq == 0) {
@@ -834,7 +949,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 const unsigned char *kst = ring + (size_t)s * STAGE;
                 const unsigned char *vst = kst + TILE;
                 float zscale = p.scale_log2, vscale = 1.f;
-                if constexpr (F8) {
+                if constexpr (F8CONV) {
                     if (nvalid > 0) {
                         const float4 am = st_scale[s];
                         zscale = p.scale_log2 * fp8_scale(am.x);
@@ -901,7 +1016,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     }
                 }
                 __syncwarp();
-                if (!F8 && lane == 0) mbar_arrive(&empty_bar[s]);
+                if (!F8CONV && lane == 0) mbar_arrive(&empty_bar[s]);
             }
             if (!wait_slot_free(kseg)) break;
 #pragma unroll
@@ -928,6 +1043,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     // keeps its registers per thread at the two-kernel level.
     constexpr int NW = FUSED ? 7 : 8;
     constexpr bool F8 = is_fp8<T>::value;
+    constexpr bool F8CONV = F8 && !(MMA && D == 128);   // FP8 tiles converted through shared memory
     constexpr int STAGE = 2 * P * D * (F8 ? 1 : (int)sizeof(T));
     AttnParams p = p0;
     // Pick the number of working consumer warps (up to NW-1) that allows the deepest ring
@@ -935,20 +1051,36 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int) + (F8 ? 16 : 0);
     int stages = 0, consumers = 0;
     for (int nw = NW - 1; nw >= 1; --nw) {   // the last consumer warp is the combiner
-        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8);
+        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);
         if (s > 32) s = 32;
         const int c = s < nw ? s : nw;
         if (c < 1) continue;
         s = s / c * c;
+        if constexpr (F8) {
+            // FP8 pages are half the bytes, so the ring is deep enough at any
+            // count; the consumers' per-page work is what limits: take the most
+            if (s >= 2 * c && c > consumers) { stages = s; consumers = c; }
+            continue;
+        }
         if (s > stages || (s == stages && c > consumers)) { stages = s; consumers = c; }
         if (nw <= 4 && stages >= 2) break;
+    }
+    if (const char *force = std::getenv("QASA_ATTN_CONSUMERS")) {   // diagnostic: fix the consumer warps
+        const int want = std::atoi(force);
+        if (want >= 1 && want <= NW - 1) {
+            const size_t fixed = attn_smem_bytes(0, STAGE, want, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
+            int s = fixed < smem_budget ? (int)((smem_budget - fixed) / per) : 0;
+            if (s > 32) s = 32;
+            s = s / want * want;
+            if (s >= 2) { stages = s; consumers = want; }
+        }
     }
     if (stages < 2) return cudaErrorInvalidConfiguration;
     p.stages = stages;
     p.consumers = consumers;
-    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8);
+    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
     auto kern = attn_kernel<T, D, P, MMA, GMAX, NW, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
