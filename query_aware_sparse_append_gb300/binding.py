@@ -164,8 +164,10 @@ class PagedKVCache:
         shape = (num_phys_pages, num_kv_heads, page_size, head_dim)
         scales = (torch.zeros((num_phys_pages, num_kv_heads, 4), dtype=torch.float32, device=device)
                   if dtype == torch.uint8 else None)
-        return cls(torch.empty(shape, dtype=dtype, device=device),
-                   torch.empty(shape, dtype=dtype, device=device),
+        # K and V carved from one allocation (V right after K): the attention
+        # kernel then fetches a page's K and V tiles with a single TMA box
+        kv = torch.empty((2,) + shape, dtype=dtype, device=device)
+        return cls(kv[0], kv[1],
                    torch.empty((num_phys_pages, num_kv_heads, 2, head_dim), dtype=dtype,
                                device=device), scales)
 

@@ -134,6 +134,44 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 //      the tile lands as [block][slot][128 B].
 //  2-D fallback: rows x head_dim, box = 128 bytes x page_size, one box per
 //      column block.
+// One map over both pools when V sits at a fixed positive offset from K
+// (e.g. both pools carved from one allocation): an extra outer dimension of
+// extent 2 and stride (v_pool - k_pool) selects K or V, so a single box brings
+// a page's K tile and V tile, laid out back to back in shared memory.
+qasa_status kv_tensor_map(CUtensorMap *map, const qasa_kv_cache *c) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return QASA_ERR_DRIVER;
+    const intptr_t kv = reinterpret_cast<intptr_t>(c->v_pool) - reinterpret_cast<intptr_t>(c->k_pool);
+    if (kv <= 0 || (kv & 15) || (unsigned long long)kv >= (1ull << 40)) return QASA_ERR_SHAPE;
+    const size_t es = elem_size(c->dtype);
+    const cuuint64_t rows = (cuuint64_t)c->num_phys_pages * c->num_kv_heads * c->page_size;
+    CUresult r;
+    if (c->dtype == QASA_DTYPE_E4M3) {
+        cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, rows, 2};
+        cuuint64_t strides[2] = {(cuuint64_t)c->head_dim, (cuuint64_t)kv};
+        cuuint32_t box[3] = {(cuuint32_t)c->head_dim, (cuuint32_t)c->page_size, 2};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c->k_pool, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                c->head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const CUtensorMapDataType t = c->dtype == QASA_DTYPE_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                      : c->dtype == QASA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const cuuint32_t boxw = (cuuint32_t)(128 / es);
+        const cuuint32_t nsub = (cuuint32_t)(c->head_dim * es / 128);
+        cuuint64_t dims[4] = {boxw, rows, nsub, 2};
+        cuuint64_t strides[3] = {(cuuint64_t)c->head_dim * es, 128, (cuuint64_t)kv};
+        cuuint32_t box[4] = {boxw, (cuuint32_t)c->page_size, nsub, 2};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(map, t, 4, c->k_pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS ? QASA_OK : QASA_ERR_DRIVER;
+}
+
 qasa_status pool_tensor_map(CUtensorMap *map, void *base, const qasa_kv_cache *c, bool three_d) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return QASA_ERR_DRIVER;
@@ -222,8 +260,12 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     if (ws_bytes < w.total || !aligned16(workspace)) return QASA_ERR_WORKSPACE;
     CUtensorMap km, vm;
     int one_box = 1;
-    if (pool_tensor_map(&km, cache->k_pool, cache, true) != QASA_OK ||
-        pool_tensor_map(&vm, cache->v_pool, cache, true) != QASA_OK) {
+    const char *no_kv = std::getenv("QASA_KV_SEPARATE");   // diagnostic: two boxes per page
+    if (!(no_kv && no_kv[0] == '1') && kv_tensor_map(&km, cache) == QASA_OK) {
+        one_box = 2;
+        vm = km;
+    } else if (pool_tensor_map(&km, cache->k_pool, cache, true) != QASA_OK ||
+               pool_tensor_map(&vm, cache->v_pool, cache, true) != QASA_OK) {
         one_box = 0;
         qasa_status st = pool_tensor_map(&km, cache->k_pool, cache, false);
         if (st != QASA_OK) return st;

@@ -468,10 +468,19 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     if (nvalid > 0) {
                         mbar_arrive_expect_tx(&full_bar[s_l], STAGE + (F8 ? 16 : 0));
                         if constexpr (F8) {
-                            // one 2-D box per code tile, and the page's scales (16 bytes)
-                            tma_load_2d(st, &kmap, &full_bar[s_l], 0, row);
-                            tma_load_2d(st + TILE, &vmap, &full_bar[s_l], 0, row);
+                            // the code tiles (one box for K and V when the pools allow),
+                            // and the page's scales (16 bytes)
+                            if (p.one_box == 2) {
+                                tma_load_3d(st, &kmap, &full_bar[s_l], 0, row, 0);
+                            } else {
+                                tma_load_2d(st, &kmap, &full_bar[s_l], 0, row);
+                                tma_load_2d(st + TILE, &vmap, &full_bar[s_l], 0, row);
+                            }
                             bulk_load(&st_scale[s_l], p.scales + (size_t)(row / P) * 4, 16, &full_bar[s_l]);
+                        } else if (p.one_box == 2) {
+                            // K and V tiles of the page in one box (the V pool sits at a
+                            // fixed offset from the K pool): one TMA operation per page
+                            tma_load_4d(st, &kmap, &full_bar[s_l], 0, row, 0, 0);
                         } else if (p.one_box) {
                             tma_load_3d(st, &kmap, &full_bar[s_l], 0, row, 0);
                             tma_load_3d(st + TILE, &vmap, &full_bar[s_l], 0, row, 0);
@@ -1049,12 +1058,16 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     // Pick the number of working consumer warps (up to NW-1) that allows the deepest ring
     // whose depth is a multiple of it (each stage owned by one consumer warp).
     const size_t per = (size_t)STAGE + 2 * sizeof(uint64_t) + sizeof(StageInfo) + sizeof(int) + (F8 ? 16 : 0);
+    // ring depth cap: 64 stages or ~200 KB of tiles in flight, whichever is less
+    // (16-bit pages reach the shared-memory limit first; FP8 pages are half the
+    // bytes and need twice the stages for the same bytes in flight)
+    constexpr int kMaxStages = (200 * 1024 / STAGE) < 64 ? (200 * 1024 / STAGE) : 64;
     int stages = 0, consumers = 0;
     for (int nw = NW - 1; nw >= 1; --nw) {   // the last consumer warp is the combiner
         const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);
-        if (s > 32) s = 32;
+        if (s > kMaxStages) s = kMaxStages;
         const int c = s < nw ? s : nw;
         if (c < 1) continue;
         s = s / c * c;
@@ -1072,7 +1085,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
         if (want >= 1 && want <= NW - 1) {
             const size_t fixed = attn_smem_bytes(0, STAGE, want, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
             int s = fixed < smem_budget ? (int)((smem_budget - fixed) / per) : 0;
-            if (s > 32) s = 32;
+            if (s > kMaxStages) s = kMaxStages;
             s = s / want * want;
             if (s >= 2) { stages = s; consumers = want; }
         }

@@ -52,7 +52,8 @@ struct AttnParams {
     int B, Hkv, G, Hq, max_pages, max_budget, num_phys;
     float scale_log2;
     int dense;
-    int one_box;       // 1: one 3-D TMA box per K/V tile; 0: one 2-D box per 128 bytes of head dim
+    int one_box;       // 2: one box per page holding its K and V tiles (kmap only);
+                       // 1: one 3-D TMA box per K/V tile; 0: one 2-D box per 128 bytes of head dim
     int stages;        // ring depth, a multiple of `consumers`
     int consumers;     // consumer warps that take pages (<= the compiled count)
     unsigned long long wait_limit_ns;

@@ -326,3 +326,18 @@ def test_full_size_sampled_units(name, seed):
         row = s[b, h]
         assert np.all(row[:k] >= 0) and np.all(np.diff(row[:k]) > 0) and np.all(row[k:] == -1)
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("env", [{"QASA_KV_SEPARATE": "1"}, {"QASA_KV_SEPARATE": "1", "QASA_TMA_2D": "1"}])
+@pytest.mark.parametrize("name,batch,seed", [("headline_8k", 3, 81), ("llama_1b3_32k", 1, 82)])
+def test_separate_kv_boxes_give_the_same_result(name, batch, seed, env, monkeypatch):
+    # pools carved from one allocation are fetched with one box per page; the
+    # per-tile 3-D boxes and the per-128-byte 2-D boxes must give the same bits
+    case = H.make_case(W.CONFIGS[name], seed=seed, batch=batch)
+    o1, s1, _, st1 = run_sparse(case)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    o2, s2, _, st2 = run_sparse(case)
+    assert st1 == 0 and st2 == 0
+    assert torch.equal(s1, s2)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
