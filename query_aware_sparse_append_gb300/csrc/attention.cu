@@ -104,8 +104,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     using MT = typename std::conditional<F8, __half, T>::type;   // q, out and MMA operand type
     constexpr int ES = F8 ? 1 : (int)sizeof(T);  // bytes per stored KV element
     constexpr int MES = (int)sizeof(MT);         // bytes per element of the tiles the consumers read
-    // FP8, d = 128, G >= 2: q.K on FP8 tensor cores straight from the (128-byte
-    // swizzled) code tiles, P.V from V fragments converted in registers;
+    // FP8, d = 128, G >= 2: the 16-bit tensor-core path on K and V fragments
+    // converted from the (128-byte swizzled) code tiles in registers;
     // otherwise FP8 tiles are converted to half copies in shared memory
     constexpr bool F8MMA = F8 && MMA && D == 128;
     constexpr bool F8CONV = F8 && !F8MMA;
@@ -693,60 +693,18 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
 
         if constexpr (MMA) {
             const int cq = lane & 3, nq = lane >> 2;
-            uint32_t qf[F8MMA ? 1 : D / 16][2];
-            // FP8: q of head nq, scaled by 2^e (largest |q| in [128, 256)), split
-            // exactly into three E4M3 terms q * 2^e = t1 + t2/16 + t3/256; the B
-            // fragments hold channels 32kk + 4cq.. (b0) and 32kk + 16 + 4cq.. (b1)
-            uint32_t q8[F8MMA ? 3 : 1][F8MMA ? D / 32 : 1][2];
-            float ie0 = 1.f, ie1 = 1.f;                  // 2^-e of heads 2cq and 2cq + 1
+            uint32_t qf[D / 16][2];
             if constexpr (F8MMA) {
-                float qv[D / 32][8];
-                float amax = 0.f;
+                // FP8: the K fragments come from code bytes 4c..4c+3 of a row, which
+                // feed MMA slots (2c, 2c+1) and (2c+8, 2c+9): q takes the same
+                // channel order, channels 16ks + 4cq .. 16ks + 4cq + 3 per lane
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    uint2 r0 = make_uint2(0, 0), r1 = make_uint2(0, 0);
-                    if (nq < G) {
-                        const MT *qr = qb + (size_t)nq * D + kk * 32 + 4 * cq;
-                        r0 = *reinterpret_cast<const uint2 *>(qr);
-                        r1 = *reinterpret_cast<const uint2 *>(qr + 16);
-                    }
-                    const uint32_t wq[4] = {r0.x, r0.y, r1.x, r1.y};
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wq[x]));
-                        qv[kk][2 * x] = f.x;
-                        qv[kk][2 * x + 1] = f.y;
-                        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-                    }
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint2 r = make_uint2(0u, 0u);
+                    if (nq < G) r = *reinterpret_cast<const uint2 *>(qb + (size_t)nq * D + ks * 16 + 4 * cq);
+                    qf[ks][0] = r.x;
+                    qf[ks][1] = r.y;
                 }
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const int e = amax > 0.f ? 7 - ilogbf(amax) : 0;
-                const float up = ldexpf(1.f, e);
-#pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    uint32_t t[3][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}};
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) {
-                        const float v = qv[kk][x] * up;                 // exact
-                        const uint32_t c1 = e4m3_from_f(v);
-                        const float r1 = (v - e4m3_to_f(c1)) * 16.f;    // exact
-                        const uint32_t c2 = e4m3_from_f(r1);
-                        const float r2 = (r1 - e4m3_to_f(c2)) * 16.f;
-                        const uint32_t c3 = e4m3_from_f(r2);
-                        t[0][x >> 2] |= c1 << (8 * (x & 3));
-                        t[1][x >> 2] |= c2 << (8 * (x & 3));
-                        t[2][x >> 2] |= c3 << (8 * (x & 3));
-                    }
-#pragma unroll
-                    for (int tt = 0; tt < 3; ++tt) {
-                        q8[tt][kk][0] = t[tt][0];
-                        q8[tt][kk][1] = t[tt][1];
-                    }
-                }
-                const float down = ldexpf(1.f, -e);
-                ie0 = __shfl_sync(0xffffffffu, down, 8 * cq);        // head 2cq: lanes 4*(2cq)..
-                ie1 = __shfl_sync(0xffffffffu, down, 8 * cq + 4);
             } else {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -810,22 +768,20 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     if (sub * 16 >= nvalid) break;
                     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
                     if constexpr (F8MMA) {
-                        // S^T = K q^T on FP8 tensor cores: the code tile rows feed the
-                        // A fragments as they are; one accumulator per q term
-                        float s3[4] = {0.f, 0.f, 0.f, 0.f};
+                        // S^T = K q^T with K fragments converted in registers: ldmatrix
+                        // on the (128-byte swizzled) code tile gives a lane the codes of
+                        // channels 4c..4c+3 of rows g and g+8 of two 16-channel blocks
 #pragma unroll
                         for (int kk = 0; kk < D / 32; ++kk) {
                             const int tok = sub * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                            uint32_t a[4];
-                            ldmatrix_x4(kbase + swz128_offset<P>(tok, 2 * kk + (lane >> 4)), a[0], a[1], a[2], a[3]);
-                            mma_e4m3_16832(sa, a, q8[0][kk][0], q8[0][kk][1]);
-                            mma_e4m3_16832(sb, a, q8[1][kk][0], q8[1][kk][1]);
-                            mma_e4m3_16832(s3, a, q8[2][kk][0], q8[2][kk][1]);
-                        }
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            sa[x] = (sa[x] + sb[x] * 0.0625f + s3[x] * 0.00390625f) * ((x & 1) ? ie1 : ie0);
-                            sb[x] = 0.f;
+                            uint32_t r[4];
+                            ldmatrix_x4(kbase + swz128_offset<P>(tok, 2 * kk + (lane >> 4)), r[0], r[1], r[2], r[3]);
+                            const uint32_t a0[4] = {e4m3x2_to_h2(r[0]), e4m3x2_to_h2(r[1]), e4m3x2_to_h2(r[0] >> 16),
+                                                    e4m3x2_to_h2(r[1] >> 16)};
+                            mma16816<MT>::run(sa, a0, qf[2 * kk][0], qf[2 * kk][1]);
+                            const uint32_t a1[4] = {e4m3x2_to_h2(r[2]), e4m3x2_to_h2(r[3]), e4m3x2_to_h2(r[2] >> 16),
+                                                    e4m3x2_to_h2(r[3] >> 16)};
+                            mma16816<MT>::run(sb, a1, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
                         }
                     } else {
 #pragma unroll

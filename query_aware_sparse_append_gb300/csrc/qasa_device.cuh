@@ -327,17 +327,6 @@ template <> struct mma16816<__nv_bfloat16> {
     }
 };
 
-// D += A(16x32, row) * B(32x8, col) on FP8 E4M3 operands, fp32 accumulators.
-// a[i]: four codes each (a0 rows 0-7 / a1 rows 8-15 at k 4c..4c+3, a2 / a3 at
-// k 16+4c..); b0 / b1: four codes of column g at k 4c.. / 16+4c...
-__device__ __forceinline__ void mma_e4m3_16832(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
