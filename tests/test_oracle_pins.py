@@ -436,3 +436,24 @@ def test_fp8_append_zero_page():
     X = np.zeros((20, 4), np.float32)
     codes, amax, lo, hi = oracle.fp8_append_replay(X, 16, [3, 17])
     assert not codes.any() and not amax.any() and not lo.any() and not hi.any()
+
+
+def test_stored_oracle_values_are_reproduced():
+    # tests/golden/tiny_decode.txt is written by tests/golden/make_golden.py from
+    # the oracle alone; any change of the oracle's arithmetic must show up here
+    import importlib.util
+    import os
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("make_golden", os.path.join(here, "make_golden.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    stored = [ln for ln in open(os.path.join(here, "tiny_decode.txt")).read().splitlines() if ln]
+    fresh = mod.golden_lines()
+    assert len(stored) == len(fresh)
+    for a, b in zip(stored, fresh):
+        if a.startswith("#") or " kept " in a:
+            assert a == b
+        else:
+            xa = [float(x) for x in a.split()[3:]]
+            xb = [float(x) for x in b.split()[3:]]
+            assert np.allclose(xa, xb, rtol=1e-12, atol=0.0), (a, b)
