@@ -68,7 +68,7 @@ typedef enum {
 typedef enum {
     QASA_OK = 0,
     QASA_ERR_NULL = 1,         /* a required pointer is NULL */
-    QASA_ERR_DTYPE = 2,        /* unknown dtype */
+    QASA_ERR_DTYPE = 2,        /* unknown dtype, or one the call does not support */
     QASA_ERR_SHAPE = 3,        /* unsupported head_dim / page_size / group / sizes */
     QASA_ERR_ALIGN = 4,        /* a device pointer is not 16-byte aligned */
     QASA_ERR_BUDGET = 5,       /* max_budget < 2 */
@@ -285,6 +285,7 @@ qasa_status qasa_sparse_decode_attention_noalloc(const qasa_kv_cache *cache, con
  *            untouched; a page with an invalid block-table entry gets 0 and
  *            sets QASA_DEVERR_PAGE_ID.  4-byte alignment suffices.
  * Other arguments as in qasa_dense_decode_attention.  Reads every key twice.
+ * 16- and 32-bit caches only (an FP8 cache returns QASA_ERR_DTYPE).
  */
 qasa_status qasa_page_attention_mass(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
                                      const int32_t *block_table, int32_t max_pages_per_seq,

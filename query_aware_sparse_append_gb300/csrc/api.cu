@@ -565,7 +565,7 @@ const char *qasa_status_string(qasa_status s) {
     switch (s) {
     case QASA_OK: return "ok";
     case QASA_ERR_NULL: return "a required pointer is NULL";
-    case QASA_ERR_DTYPE: return "unknown dtype";
+    case QASA_ERR_DTYPE: return "unknown dtype, or a dtype this call does not support";
     case QASA_ERR_SHAPE: return "unsupported shape (head_dim, page_size, group size or sizes)";
     case QASA_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
     case QASA_ERR_BUDGET: return "max_budget must be at least 2";

@@ -169,3 +169,35 @@ def test_fp8_zero_pages_and_empty_sequences():
     out, sel, scores = _decode(case)
     _check_decode(case, None, _units(case), out, sel, scores)
     assert np.all(H.gpu_out64(out, "e4m3")[0] == 0)
+
+
+def test_fp8_through_the_other_entry_points(monkeypatch):
+    # the single-launch request falls back to two launches for FP8 caches; the
+    # workspace-free and host-buffer calls give the same bits; the page-mass
+    # instrumentation refuses FP8 caches with QASA_ERR_DTYPE
+    qasa = _qasa()
+    case = H.make_case(_fp8("headline_8k"), seed=69, batch=4)
+    ref_out, ref_sel, _ = _decode(case)
+    monkeypatch.setenv("QASA_SINGLE_LAUNCH", "1")
+    o1, s1, _ = _decode(case)
+    monkeypatch.delenv("QASA_SINGLE_LAUNCH")
+    assert torch.equal(s1, ref_sel) and torch.equal(o1.view(torch.int16), ref_out.view(torch.int16))
+
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(ref_out)
+    sel = torch.empty_like(ref_sel)
+    assert qasa.sparse_decode_attention_noalloc(case.cache, case.q_dev, case.bt, case.lens_dev, case.budget_dev,
+                                                case.max_budget, out, sel, status=status) == 0
+    out_h = torch.empty(tuple(ref_out.shape), dtype=ref_out.dtype).pin_memory()
+    sel_h = torch.empty(tuple(ref_sel.shape), dtype=torch.int32).pin_memory()
+    qasa.sparse_decode_attention_host(case.cache, case.q_dev.cpu().pin_memory(), case.bt.cpu().pin_memory(),
+                                      case.lens_dev.cpu().pin_memory(), case.budget_dev.cpu().pin_memory(),
+                                      case.max_budget, out_h, sel_h, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(sel, ref_sel) and torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(sel_h, ref_sel.cpu()) and torch.equal(out_h.view(torch.int16), ref_out.cpu().view(torch.int16))
+
+    with pytest.raises(qasa.QasaError) as err:
+        qasa.page_attention_mass(case.cache, case.q_dev, case.bt, case.lens_dev)
+    assert "dtype" in str(err.value)
