@@ -69,26 +69,22 @@ static cudaError_t launch_select_t(const SelectParams &p, int units, cudaStream_
 
 cudaError_t launch_select(qasa_dtype dt, int D, const SelectParams &p, int units,
                           cudaStream_t stream) {
-    const bool mma = dt != QASA_DTYPE_F32 && p.G >= 2;
-    if (dt == QASA_DTYPE_E4M3) {
-        if (mma) return D == 64 ? launch_select_t<fp8e4m3, 64, true, 1>(p, units, stream)
-                                : launch_select_t<fp8e4m3, 128, true, 1>(p, units, stream);
-        return D == 64 ? launch_select_t<fp8e4m3, 64, false, 1>(p, units, stream)
-                       : launch_select_t<fp8e4m3, 128, false, 1>(p, units, stream);
-    }
-    if (dt == QASA_DTYPE_F32)
+    // tensor-core scoring for 16-bit and FP8 boxes at every group size (unused
+    // query heads of the 8-wide MMA are zero); FFMA for fp32
+    switch (dt) {
+    case QASA_DTYPE_F32:
         return D == 64 ? launch_select_t<float, 64, false, 8>(p, units, stream)
                        : launch_select_t<float, 128, false, 8>(p, units, stream);
-    if (dt == QASA_DTYPE_F16) {
-        if (mma) return D == 64 ? launch_select_t<__half, 64, true, 1>(p, units, stream)
-                                : launch_select_t<__half, 128, true, 1>(p, units, stream);
-        return D == 64 ? launch_select_t<__half, 64, false, 1>(p, units, stream)
-                       : launch_select_t<__half, 128, false, 1>(p, units, stream);
+    case QASA_DTYPE_E4M3:
+        return D == 64 ? launch_select_t<fp8e4m3, 64, true, 1>(p, units, stream)
+                       : launch_select_t<fp8e4m3, 128, true, 1>(p, units, stream);
+    case QASA_DTYPE_F16:
+        return D == 64 ? launch_select_t<__half, 64, true, 1>(p, units, stream)
+                       : launch_select_t<__half, 128, true, 1>(p, units, stream);
+    default:
+        return D == 64 ? launch_select_t<__nv_bfloat16, 64, true, 1>(p, units, stream)
+                       : launch_select_t<__nv_bfloat16, 128, true, 1>(p, units, stream);
     }
-    if (mma) return D == 64 ? launch_select_t<__nv_bfloat16, 64, true, 1>(p, units, stream)
-                            : launch_select_t<__nv_bfloat16, 128, true, 1>(p, units, stream);
-    return D == 64 ? launch_select_t<__nv_bfloat16, 64, false, 1>(p, units, stream)
-                   : launch_select_t<__nv_bfloat16, 128, false, 1>(p, units, stream);
 }
 
 }  // namespace qasa

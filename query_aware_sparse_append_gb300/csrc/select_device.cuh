@@ -16,7 +16,8 @@
 // written as ascending logical ids.
 //
 // Two scoring paths:
-//  * tensor cores (16-bit KV, G >= 2).  Because lo <= hi, the per-channel
+//  * tensor cores (16-bit and FP8 KV, any group size: the unused query heads
+//    of the 8-wide MMA are zero).  Because lo <= hi, the per-channel
 //    maximum equals q+ * hi + q- * lo with q+ = max(q,0), q- = min(q,0): the
 //    scores of 16 pages are one [16 x 2d] x [2d x 8] contraction, run as
 //    m16n8k16 MMAs with the box rows (lo | hi, contiguous) as the A operand and
@@ -24,8 +25,8 @@
 //    Each lane loads 16-byte chunks of the box rows straight into A-fragment
 //    registers: the channel order inside the contraction is permuted
 //    consistently for A and B, which the sum does not see.
-//  * FFMA (G == 1, or fp32 KV): a warp scores a few pages at a time with
-//    16-byte loads and shuffle reductions.
+//  * FFMA (fp32 KV): a warp scores a few pages at a time with 16-byte loads
+//    and shuffle reductions.
 //
 // Selection: radix select (4 passes of 8 bits, warp-aggregated shared-memory
 // histograms) finds the key of the (k-2)-th best candidate; an ordered group
@@ -89,7 +90,7 @@ __device__ __forceinline__ int group_excl_scan(const Grp &g, int v, int *warp_to
 
 // ----------------------------------------------------------- scoring paths
 
-// Tensor-core scores of all N pages into sc[] (16-bit KV, 2 <= G <= 8).
+// Tensor-core scores of all N pages into sc[] (16-bit KV, 1 <= G <= 8).
 template <typename T, int D, class Grp>
 __device__ void score_pages_mma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
     constexpr int J = D / 16;          // 16-byte chunks per lane per box row (2D elements / 8 / 4 lanes)
@@ -184,7 +185,7 @@ struct BoxStageShape {
 };
 
 // Tensor-core scores of all N pages into sc[] from staged box rows (16-bit KV,
-// 2 <= G <= 8).  phase_bits holds the parity of this warp's slot barriers and
+// 1 <= G <= 8).  phase_bits holds the parity of this warp's slot barriers and
 // persists across units.  Every copy issued here is waited for before return.
 template <typename T, int D, class Grp>
 __device__ void score_pages_mma_staged(const Grp &grp, const SelectParams &p, int b, int h, int N,
@@ -370,76 +371,7 @@ __device__ void score_pages_fp8_mma(const Grp &grp, const SelectParams &p, int b
     }
 }
 
-// FP8 boxes, one query head per KV head (FFMA): lane groups of D/8 lanes hold
-// one box row (16 codes per lane); NB rows per round with all loads in flight.
-template <int D, int GMAX, class Grp>
-__device__ void score_pages_fp8_ffma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
-    constexpr int LPR = D / 8;                   // 2D codes per row / 16 per lane
-    constexpr int RPW = 32 / LPR;
-    constexpr int NB = 4;
-    const int lane = grp.lane(), warp = grp.warp();
-    const int rsub = lane / LPR, csub = lane % LPR;
-    const int G = p.G;
-    float qq[GMAX][16];
-    const __half *qb = static_cast<const __half *>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
-#pragma unroll
-    for (int g = 0; g < GMAX; ++g)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int idx = csub * 16 + e;
-            float v = 0.f;
-            if (g < G) {
-                const float qv = __half2float(qb[(size_t)g * D + (idx % D)]);
-                v = idx < D ? fminf(qv, 0.f) : fmaxf(qv, 0.f);
-            }
-            qq[g][e] = v;
-        }
-    const uint8_t *bounds = static_cast<const uint8_t *>(p.bounds);
-    const int32_t *bt = p.block_table + (size_t)b * p.max_pages;
-    const int npass = (N + RPW - 1) / RPW;
-    for (int pass0 = warp; pass0 < npass; pass0 += Grp::warps * NB) {
-        int page[NB];
-        bool ok[NB];
-        uint4 raw[NB];
-        float am[NB];
-#pragma unroll
-        for (int q = 0; q < NB; ++q) {
-            page[q] = (pass0 + q * Grp::warps) * RPW + rsub;
-            const bool in = pass0 + q * Grp::warps < npass && page[q] < N;
-            const int ph = in ? bt[page[q]] : -1;
-            ok[q] = ph >= 0 && ph < p.num_phys;
-            if (in && !ok[q] && csub == 0 && p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
-            const size_t e = (size_t)(ok[q] ? ph : 0) * p.Hkv + h;
-            raw[q] = ok[q] ? ld_global_nc_v4(bounds + e * 2 * D + csub * 16) : make_uint4(0, 0, 0, 0);
-            am[q] = ok[q] ? p.scales[e * 4] : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < NB; ++q) {
-            if (pass0 + q * Grp::warps >= npass) break;      // warp-uniform
-            const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
-            float acc[GMAX];
-#pragma unroll
-            for (int g = 0; g < GMAX; ++g) acc[g] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float f = e4m3_to_f((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
-#pragma unroll
-                for (int g = 0; g < GMAX; ++g) acc[g] = fmaf(qq[g][e], f, acc[g]);
-            }
-            float best = -INFINITY;
-#pragma unroll
-            for (int g = 0; g < GMAX; ++g) {
-                float a = acc[g];
-#pragma unroll
-                for (int off = 1; off < LPR; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-                if (g < G) best = fmaxf(best, a);
-            }
-            if (csub == 0 && page[q] < N) sc[page[q]] = ok[q] ? __fmul_rn(best, fp8_scale(am[q])) : -INFINITY;
-        }
-    }
-}
-
-// FFMA scores (any dtype, G <= GMAX).
+// FFMA scores (fp32 boxes, G <= GMAX).
 template <typename T, int D, int GMAX, class Grp>
 __device__ void score_pages_ffma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
     constexpr int EPC = chunk16<T>::n;
@@ -543,8 +475,7 @@ __device__ void select_unit(const Grp &grp, const SelectParams &p, int u, float 
     const bool need_scores = (k < N) || (p.scores_out != nullptr);
     if (need_scores) {
         if constexpr (is_fp8<T>::value) {
-            if constexpr (MMA) score_pages_fp8_mma<D>(grp, p, b, h, N, sc);
-            else score_pages_fp8_ffma<D, GMAX>(grp, p, b, h, N, sc);
+            score_pages_fp8_mma<D>(grp, p, b, h, N, sc);
         } else if constexpr (MMA) {
             if (stage) score_pages_mma_staged<T, D>(grp, p, b, h, N, sc, *stage, *phase_bits);
             else score_pages_mma<T, D>(grp, p, b, h, N, sc);
