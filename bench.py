@@ -583,9 +583,12 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     rebuild_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in evr[1:])
 
-    # ---- end to end through the C-ABI host-buffer call: per step, the H2D
-    # copies of q, block table, lengths and budgets from pinned host memory, the
-    # decode step, and the D2H copies of the output and the kept ids
+    # ---- end to end through the C-ABI host-buffer call: per step, q, block
+    # table, lengths and budgets come from pinned host memory and the output and
+    # kept ids go back to it.  Direct form (the default where the device can
+    # address the pinned buffers): the kernels read and write host memory over
+    # the CPU-GPU link themselves.  Staged form (QASA_HOST_DIRECT=0): H2D copies,
+    # the decode step, D2H copies.  Both are timed; e2e.value is the default.
     q_h = wl.q_dev.cpu().pin_memory()
     lens_h = wl.lens_dev.cpu().pin_memory()
     bud_h = wl.budget_dev.cpu().pin_memory()
@@ -594,51 +597,67 @@ def run_ours(args):
     sel_h = torch.empty(sel.shape, dtype=sel.dtype).pin_memory()
     host_ws = qasa.alloc_host_workspace(wl.cache, B, Hq, maxp, max_budget, device=dev)
 
-    def e2e_step():
-        qasa.sparse_decode_attention_host(wl.cache, q_h, bt_h, lens_h, bud_h, max_budget, out_h, sel_h,
-                                          workspace=host_ws, status=status)
+    def time_host_call(direct):
+        old = os.environ.get("QASA_HOST_DIRECT")
+        os.environ["QASA_HOST_DIRECT"] = "1" if direct else "0"
+        try:
+            form = "direct" if qasa.host_call_is_direct(q_h, bt_h, lens_h, bud_h, out_h, sel_h) else "staged"
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e2e_eager = []
-    for _ in range(args.steps):
-        flush.zero_()
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        e2e_eager.append(1000.0 * (time.perf_counter() - t0))
-    # the same call captured once in a CUDA graph (copies and kernels are all
-    # stream work; the host buffers stay fixed, a server rewrites them per step)
-    e2e_mode = "eager"
-    try:
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(cap):
-            e2e_step()                       # warm the capture stream
-            torch.cuda.synchronize(dev)
-            with torch.cuda.graph(graph, stream=cap):
+            def e2e_step():
+                qasa.sparse_decode_attention_host(wl.cache, q_h, bt_h, lens_h, bud_h, max_budget, out_h, sel_h,
+                                                  workspace=host_ws, status=status)
+
+            for _ in range(2):
                 e2e_step()
-        torch.cuda.synchronize(dev)
-        e2e_step_graph = graph.replay
-        for _ in range(2):
-            e2e_step_graph()
-        torch.cuda.synchronize(dev)
-        e2e_step = e2e_step_graph
-        e2e_mode = "cuda_graph"
-    except Exception as exc:                 # capture refused: keep the eager number
-        e2e_mode = "eager (graph capture failed: %s)" % str(exc).splitlines()[0][:120]
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush.zero_()
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        e2e_ms.append(1000.0 * (time.perf_counter() - t0))
-    e2e_mean = max_over_ranks(statistics.mean(e2e_ms), dev)
+            torch.cuda.synchronize(dev)
+            eager = []
+            for _ in range(args.steps):
+                flush.zero_()
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+                e2e_step()
+                torch.cuda.synchronize(dev)
+                eager.append(1000.0 * (time.perf_counter() - t0))
+            # the same call captured once in a CUDA graph (copies and kernels are
+            # all stream work; the host buffers stay fixed, a server rewrites them
+            # per step)
+            mode = "eager"
+            try:
+                graph = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream(dev)
+                cap.wait_stream(torch.cuda.current_stream(dev))
+                with torch.cuda.stream(cap):
+                    e2e_step()               # warm the capture stream
+                    torch.cuda.synchronize(dev)
+                    with torch.cuda.graph(graph, stream=cap):
+                        e2e_step()
+                torch.cuda.synchronize(dev)
+                for _ in range(2):
+                    graph.replay()
+                torch.cuda.synchronize(dev)
+                e2e_step = graph.replay
+                mode = "cuda_graph"
+            except Exception as exc:         # capture refused: keep the eager number
+                mode = "eager (graph capture failed: %s)" % str(exc).splitlines()[0][:120]
+            ms = []
+            for _ in range(args.steps):
+                flush.zero_()
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+                e2e_step()
+                torch.cuda.synchronize(dev)
+                ms.append(1000.0 * (time.perf_counter() - t0))
+            return {"transfer": form, "mode": mode, "ms_per_step": max_over_ranks(statistics.mean(ms), dev),
+                    "eager_ms_per_step": statistics.mean(eager)}
+        finally:
+            if old is None:
+                del os.environ["QASA_HOST_DIRECT"]
+            else:
+                os.environ["QASA_HOST_DIRECT"] = old
+
+    e2e_staged = time_host_call(False)
+    e2e_default = time_host_call(os.environ.get("QASA_HOST_DIRECT", "1") != "0")
+    e2e_mean = e2e_default["ms_per_step"]
     h2d = sum(x.numel() * x.element_size() for x in (q_h, lens_h, bud_h, bt_h))
     d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
 
@@ -721,8 +740,8 @@ def run_ours(args):
                              "frac": rebuild_b / (rebuild_ms * 1e-3) / 1e9 / peak},
         "cpu_baseline": cpu,
         "e2e": {"value": world * B / (e2e_mean * 1e-3), "unit": "queries/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
-                "mode": e2e_mode, "eager_ms_per_step": statistics.mean(e2e_eager)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, **e2e_default,
+                "staged": {**e2e_staged, "queries_per_s": world * B / (e2e_staged["ms_per_step"] * 1e-3)}},
         "gpu_launches": (1 if single else 2) * args.steps,
         "clocks": clocks.summary(),
     }

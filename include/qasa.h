@@ -315,19 +315,31 @@ qasa_status qasa_page_hit_rate(const qasa_kv_cache *cache, const float *mass, in
 
 /*
  * The decode step with its per-call inputs and outputs in HOST memory (the
- * KV cache stays on the device): enqueues on `stream` one cudaMemcpyAsync per
- * input (q, block table, seq_lens, budget_pages) into `workspace`, the step of
- * qasa_sparse_decode_attention, and one copy per output (out, selected) back.
- * The paper has no counterpart; this is the call a host-driven server makes.
+ * KV cache stays on the device).  The paper has no counterpart; this is the
+ * call a host-driven server makes.  Two transfer forms, same kernels, same bits:
+ *   direct  every host buffer is page-locked memory the device can address
+ *           at the same pointer (cudaHostAlloc / cudaHostRegister on a device
+ *           with cudaDevAttrCanUseHostPointerForRegisteredMem, e.g. a
+ *           Grace-Blackwell node over NVLink-C2C): the kernels of
+ *           qasa_sparse_decode_attention read q, the block table, lengths and
+ *           budgets and write out and selected in host memory themselves, with
+ *           no copy launched;
+ *   staged  otherwise, or when the environment sets QASA_HOST_DIRECT=0: one
+ *           cudaMemcpyAsync per input into `workspace`, the step, and one copy
+ *           per output back, all on `stream`.
  *   q_host, out_host            [batch][num_q_heads][head_dim] (f16 for FP8 KV)
  *   block_table_host            [batch][max_pages_per_seq] int32
  *   seq_lens_host, budget_pages_host  [batch] int32
  *   selected_host               [batch][num_kv_heads][max_budget] int32
  *   workspace                   device memory of qasa_host_decode_workspace_size
  *                               bytes, 256-byte aligned (scratch, no initialisation)
- * The outputs are valid once the stream has been synchronised.  Host buffers
- * should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to be
- * asynchronous.  Errors as in qasa_sparse_decode_attention.
+ * The outputs are valid once the stream has been synchronised; the host must
+ * not touch the buffers before that.  Pageable host buffers take the staged
+ * form (their copies are synchronous to the host).  Errors as in
+ * qasa_sparse_decode_attention.
+ *
+ * qasa_host_call_is_direct returns 1 when a call with these six buffers takes
+ * the direct form, 0 when it takes the staged form.
  */
 size_t qasa_host_decode_workspace_size(int32_t batch, int32_t num_q_heads, const qasa_kv_cache *cache,
                                        int32_t max_pages_per_seq, int32_t max_budget);
@@ -338,6 +350,9 @@ qasa_status qasa_sparse_decode_attention_host(const qasa_kv_cache *cache, const 
                                               float scale, void *out_host, int32_t *selected_host,
                                               void *workspace, size_t workspace_bytes, int32_t batch,
                                               int32_t *device_status, cudaStream_t stream);
+int32_t qasa_host_call_is_direct(const void *q_host, const int32_t *block_table_host,
+                                 const int32_t *seq_lens_host, const int32_t *budget_pages_host,
+                                 const void *out_host, const int32_t *selected_host);
 
 /* Static description of a status code. */
 const char *qasa_status_string(qasa_status status);

@@ -74,6 +74,8 @@ _lib.qasa_host_decode_workspace_size.restype = ctypes.c_size_t
 _lib.qasa_sparse_decode_attention_host.argtypes = [_C, _P, _I, _P, _I, _P, _P, _I, ctypes.c_float, _P, _P, _P,
                                                    ctypes.c_size_t, _I, _P, _P]
 _lib.qasa_sparse_decode_attention_host.restype = _I
+_lib.qasa_host_call_is_direct.argtypes = [_P] * 6
+_lib.qasa_host_call_is_direct.restype = _I
 _lib.qasa_status_string.argtypes = [_I]
 _lib.qasa_status_string.restype = ctypes.c_char_p
 _lib.qasa_version.restype = _I
@@ -83,7 +85,7 @@ EXPORTED = ("qasa_kv_append", "qasa_decode_workspace_size", "qasa_select_pages",
             "qasa_dense_decode_attention", "qasa_sparse_decode_attention_noalloc",
             "qasa_rebuild_page_bounds", "qasa_page_attention_mass", "qasa_page_hit_rate",
             "qasa_host_decode_workspace_size", "qasa_sparse_decode_attention_host",
-            "qasa_status_string", "qasa_version")
+            "qasa_host_call_is_direct", "qasa_status_string", "qasa_version")
 
 
 class QasaError(RuntimeError):
@@ -327,8 +329,10 @@ def sparse_decode_attention_host(cache: PagedKVCache, q_host: torch.Tensor, bloc
                                  out_host: torch.Tensor, selected_host: torch.Tensor,
                                  workspace: Optional[torch.Tensor] = None, scale: Optional[float] = None,
                                  status: Optional[torch.Tensor] = None, stream=None) -> int:
-    """The decode step with host (preferably pinned) inputs and outputs; the
-    copies and kernels are enqueued on the stream (synchronise before reading)."""
+    """The decode step with host (preferably pinned) inputs and outputs: the
+    kernels access pinned buffers in place where the device can address them,
+    else the copies and kernels are enqueued on the stream (synchronise before
+    reading either way)."""
     B, Hq = int(q_host.shape[0]), int(q_host.shape[1])
     maxp = int(block_table_host.shape[1])
     if workspace is None:
@@ -340,6 +344,14 @@ def sparse_decode_attention_host(cache: PagedKVCache, q_host: torch.Tensor, bloc
         _ptr(workspace), workspace.numel(), B, _ptr(status), _stream(stream))
     _check(code, "qasa_sparse_decode_attention_host")
     return code
+
+
+def host_call_is_direct(q_host: torch.Tensor, block_table_host: torch.Tensor, seq_lens_host: torch.Tensor,
+                        budget_host: torch.Tensor, out_host: torch.Tensor, selected_host: torch.Tensor) -> bool:
+    """True when sparse_decode_attention_host with these buffers lets the
+    kernels read and write them in host memory (no copies launched)."""
+    return bool(_lib.qasa_host_call_is_direct(*(_ptr(t) for t in (q_host, block_table_host, seq_lens_host,
+                                                                  budget_host, out_host, selected_host))))
 
 
 def dense_decode_attention(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,

@@ -1,13 +1,17 @@
 // hostio.cu -- the decode step with its inputs and outputs in host memory.
 //
-// qasa_sparse_decode_attention_host stages the step's per-call inputs (queries,
-// block table, lengths, budgets) from host buffers into a device workspace,
-// runs the decode step of qasa_sparse_decode_attention, and copies the outputs
-// (attention output and kept page ids) back, all enqueued on one stream: one
-// call for a host that keeps its per-step tensors on the CPU side.  The KV
-// cache itself stays in device memory.  Copies are plain cudaMemcpyAsync, one
-// per buffer; with page-locked host buffers they overlap nothing but are
-// asynchronous to the host.
+// qasa_sparse_decode_attention_host runs the decode step of
+// qasa_sparse_decode_attention for a host that keeps its per-step tensors
+// (queries, block table, lengths, budgets; output and kept page ids) on the
+// CPU side; the KV cache stays in device memory.  Where the device can address
+// every one of those page-locked buffers at its host pointer (Grace-Blackwell:
+// coherent NVLink-C2C), the kernels read and write them in place and no copy
+// is launched: the transfers ride on the kernels' own loads and stores.
+// Otherwise the inputs are staged into the device workspace with one
+// cudaMemcpyAsync per buffer and the outputs copied back the same way, all on
+// one stream.
+#include <cstdlib>
+
 #include "qasa_launch.h"
 
 namespace {
@@ -33,6 +37,28 @@ bool host_layout(int batch, int num_q_heads, const qasa_kv_cache *cache, int max
     l->out = l->budget + align256((size_t)batch * 4);
     l->sel = l->out + align256(qbytes);
     l->total = l->sel + align256((size_t)batch * cache->num_kv_heads * max_budget * 4);
+    return true;
+}
+
+// Direct form: the device can dereference every host buffer at its host
+// address (page-locked memory known to the driver, on a device that accepts
+// host pointers for it), unless QASA_HOST_DIRECT is "0".
+bool host_memory_direct(const void *a, const void *b, const void *c, const void *d, const void *e, const void *f) {
+    const char *v = std::getenv("QASA_HOST_DIRECT");
+    if (v && v[0] == '0') return false;
+    int dev = 0, ok = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&ok, cudaDevAttrCanUseHostPointerForRegisteredMem, dev) != cudaSuccess || !ok)
+        return false;
+    const void *ptrs[] = {a, b, c, d, e, f};
+    for (const void *p : ptrs) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        if (attr.type != cudaMemoryTypeHost || attr.devicePointer != p) return false;
+    }
     return true;
 }
 
@@ -62,6 +88,14 @@ extern "C" qasa_status qasa_sparse_decode_attention_host(
     if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return QASA_ERR_WORKSPACE;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
+    if (host_memory_direct(q_host, block_table_host, seq_lens_host, budget_pages_host, out_host, selected_host)) {
+        // the kernels read the inputs and write the outputs in host memory
+        // themselves (coherent device access to host memory, e.g. NVLink-C2C)
+        return qasa_sparse_decode_attention(cache, q_host, num_q_heads, block_table_host, max_pages_per_seq,
+                                            seq_lens_host, budget_pages_host, max_budget, scale, out_host,
+                                            selected_host, nullptr, ws + l.decode, l.q, batch, device_status,
+                                            stream);
+    }
     const size_t qbytes = (size_t)batch * num_q_heads * cache->head_dim * elem_bytes_q(cache);
     const size_t btbytes = (size_t)batch * max_pages_per_seq * 4;
     const size_t selbytes = (size_t)batch * cache->num_kv_heads * max_budget * 4;
@@ -81,4 +115,13 @@ extern "C" qasa_status qasa_sparse_decode_attention_host(
         cudaMemcpyAsync(selected_host, ws + l.sel, selbytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
         return QASA_ERR_CUDA;
     return QASA_OK;
+}
+
+extern "C" int32_t qasa_host_call_is_direct(const void *q_host, const int32_t *block_table_host,
+                                            const int32_t *seq_lens_host, const int32_t *budget_pages_host,
+                                            const void *out_host, const int32_t *selected_host) {
+    if (!q_host || !block_table_host || !seq_lens_host || !budget_pages_host || !out_host || !selected_host)
+        return 0;
+    return host_memory_direct(q_host, block_table_host, seq_lens_host, budget_pages_host, out_host, selected_host)
+               ? 1 : 0;
 }
