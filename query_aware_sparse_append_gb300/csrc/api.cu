@@ -83,6 +83,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // refused (not every CTA can be resident); the caller falls back to two.
 constexpr qasa_status QASA_ERR_COOPERATIVE = static_cast<qasa_status>(100);
 
+// Fewest kept pages per attention CTA before the grid shrinks below one CTA per SM.
+constexpr int kMinPagesPerCta = 8;
+
 // The decode step runs as two kernels (selection, then attention) unless
 // QASA_SINGLE_LAUNCH=1 asks for the single cooperative launch.  On GB300 the
 // two-kernel form is faster for every measured workload: inside one launch
@@ -318,10 +321,20 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     size_t budget = smem_optin();
     if (budget == 0) return QASA_ERR_CUDA;
     budget = budget > 1024 ? budget - 1024 : budget;   // leave room for static shared memory
+    // Small batches: at least kMinPagesPerCta pages per CTA for the most pages
+    // the batch can attend to, so a unit is not spread over dozens of CTAs
+    // whose partials its last arriver then merges one after another.  (The
+    // workspace is sized for the full grid; fewer CTAs use fewer slots.)
+    int attn_grid = grid;
+    if (!fused) {
+        const long long most = (long long)units * (dense ? max_pages : max_budget);
+        const long long want = (most + kMinPagesPerCta - 1) / kMinPagesPerCta;
+        if (want < attn_grid) attn_grid = want < 1 ? 1 : (int)want;
+    }
     cudaError_t e = fused ? launch_fused_decode(cache->dtype, cache->head_dim, cache->page_size, km, vm, p,
                                                 grid, budget, stream)
-                          : launch_attention(cache->dtype, cache->head_dim, cache->page_size, km, vm, p, grid,
-                                             budget, pdl, stream);
+                          : launch_attention(cache->dtype, cache->head_dim, cache->page_size, km, vm, p,
+                                             attn_grid, budget, pdl, stream);
     if (e == cudaErrorInvalidConfiguration) return QASA_ERR_SHAPE;
     if (e == cudaErrorCooperativeLaunchTooLarge) {   // not every CTA could be resident: two launches
         (void)cudaGetLastError();

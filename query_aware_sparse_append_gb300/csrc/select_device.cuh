@@ -90,9 +90,11 @@ __device__ __forceinline__ int group_excl_scan(const Grp &g, int v, int *warp_to
 
 // ----------------------------------------------------------- scoring paths
 
-// Tensor-core scores of all N pages into sc[] (16-bit KV, 1 <= G <= 8).
+// Tensor-core scores of the pages of 16-page tiles [t_begin, t_end) (pages
+// below N) into sc[] (16-bit KV, 1 <= G <= 8).
 template <typename T, int D, class Grp>
-__device__ void score_pages_mma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
+__device__ void score_pages_mma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc,
+                                int t_begin, int t_end) {
     constexpr int J = D / 16;          // 16-byte chunks per lane per box row (2D elements / 8 / 4 lanes)
     const int lane = grp.lane(), warp = grp.warp();
     const int c = lane & 3, n = lane >> 2;
@@ -115,18 +117,19 @@ __device__ void score_pages_mma(const Grp &grp, const SelectParams &p, int b, in
 
     const T *bounds = static_cast<const T *>(p.bounds);
     const int32_t *bt = p.block_table + (size_t)b * p.max_pages;
-    const int ntiles = (N + 15) >> 4;
     // the block-table entries of a warp's next tile are loaded while its
     // current tile's boxes are in flight (one dependent round trip per tile)
-    int nph0 = warp * 16 + n < N ? bt[warp * 16 + n] : -1;
-    int nph1 = warp * 16 + n + 8 < N ? bt[warp * 16 + n + 8] : -1;
-    for (int t = warp; t < ntiles; t += Grp::warps) {
+    const int tw = t_begin + warp;
+    int nph0 = tw < t_end && tw * 16 + n < N ? bt[tw * 16 + n] : -1;
+    int nph1 = tw < t_end && tw * 16 + n + 8 < N ? bt[tw * 16 + n + 8] : -1;
+    for (int t = tw; t < t_end; t += Grp::warps) {
         const int r0 = t * 16 + n, r1 = r0 + 8;
         const int ph0 = nph0, ph1 = nph1;
         {
+            const bool more = t + Grp::warps < t_end;
             const int q0 = (t + Grp::warps) * 16 + n;
-            nph0 = q0 < N ? bt[q0] : -1;
-            nph1 = q0 + 8 < N ? bt[q0 + 8] : -1;
+            nph0 = more && q0 < N ? bt[q0] : -1;
+            nph1 = more && q0 + 8 < N ? bt[q0 + 8] : -1;
         }
         const bool ok0 = ph0 >= 0 && ph0 < p.num_phys, ok1 = ph1 >= 0 && ph1 < p.num_phys;
         if (((r0 < N && !ok0) || (r1 < N && !ok1)) && p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
@@ -292,7 +295,8 @@ __device__ void score_pages_mma_staged(const Grp &grp, const SelectParams &p, in
 // k = c + 4m of the [lo | hi] row, i.e. half chunks 2k and 2k+1, which feed MMA
 // slots 2m and 2m+1; the q fragments use the same channel order.
 template <int D, class Grp>
-__device__ void score_pages_fp8_mma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
+__device__ void score_pages_fp8_mma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc,
+                                    int t_begin, int t_end) {
     constexpr int J = D / 16;          // MMA slots per lane per box row, as in the 16-bit path
     constexpr int JC = J / 2;          // 16-byte code chunks per lane per box row
     const int lane = grp.lane(), warp = grp.warp();
@@ -315,16 +319,17 @@ __device__ void score_pages_fp8_mma(const Grp &grp, const SelectParams &p, int b
 
     const uint8_t *bounds = static_cast<const uint8_t *>(p.bounds);
     const int32_t *bt = p.block_table + (size_t)b * p.max_pages;
-    const int ntiles = (N + 15) >> 4;
-    int nph0 = warp * 16 + n < N ? bt[warp * 16 + n] : -1;
-    int nph1 = warp * 16 + n + 8 < N ? bt[warp * 16 + n + 8] : -1;
-    for (int t = warp; t < ntiles; t += Grp::warps) {
+    const int tw = t_begin + warp;
+    int nph0 = tw < t_end && tw * 16 + n < N ? bt[tw * 16 + n] : -1;
+    int nph1 = tw < t_end && tw * 16 + n + 8 < N ? bt[tw * 16 + n + 8] : -1;
+    for (int t = tw; t < t_end; t += Grp::warps) {
         const int r0 = t * 16 + n, r1 = r0 + 8;
         const int ph0 = nph0, ph1 = nph1;
         {
+            const bool more = t + Grp::warps < t_end;
             const int q0 = (t + Grp::warps) * 16 + n;
-            nph0 = q0 < N ? bt[q0] : -1;
-            nph1 = q0 + 8 < N ? bt[q0 + 8] : -1;
+            nph0 = more && q0 < N ? bt[q0] : -1;
+            nph1 = more && q0 + 8 < N ? bt[q0 + 8] : -1;
         }
         const bool ok0 = ph0 >= 0 && ph0 < p.num_phys, ok1 = ph1 >= 0 && ph1 < p.num_phys;
         if (((r0 < N && !ok0) || (r1 < N && !ok1)) && p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
@@ -371,14 +376,17 @@ __device__ void score_pages_fp8_mma(const Grp &grp, const SelectParams &p, int b
     }
 }
 
-// FFMA scores (fp32 boxes, G <= GMAX).
+// FFMA scores (fp32 boxes, G <= GMAX) of the pages of 16-page tiles
+// [t_begin, t_end) below N.
 template <typename T, int D, int GMAX, class Grp>
-__device__ void score_pages_ffma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc) {
+__device__ void score_pages_ffma(const Grp &grp, const SelectParams &p, int b, int h, int N, float *sc,
+                                 int t_begin, int t_end) {
     constexpr int EPC = chunk16<T>::n;
     constexpr int CPR = 2 * D / EPC;             // chunks per box row (lo | hi)
     constexpr int LPR = CPR < 32 ? CPR : 32;     // lanes per row
     constexpr int CPL = CPR / LPR;               // chunks per lane
     constexpr int RPW = 32 / LPR;                // rows per warp pass
+    static_assert(16 % RPW == 0, "a tile holds whole passes");
     const int lane = grp.lane(), warp = grp.warp();
     const int rsub = lane / LPR, csub = lane % LPR;
     const int G = p.G;
@@ -402,11 +410,12 @@ __device__ void score_pages_ffma(const Grp &grp, const SelectParams &p, int b, i
 
     const T *bounds = static_cast<const T *>(p.bounds);
     const int32_t *bt = p.block_table + (size_t)b * p.max_pages;
-    const int npass = (N + RPW - 1) / RPW;
+    const int pass_begin = t_begin * 16 / RPW;
+    const int npass = (min(N, t_end * 16) + RPW - 1) / RPW;
     // NB passes per round: their block-table loads, then their box loads, are
     // all in flight together (two round trips per NB passes, not per pass)
     constexpr int NB = 4;
-    for (int pass0 = warp; pass0 < npass; pass0 += Grp::warps * NB) {
+    for (int pass0 = pass_begin + warp; pass0 < npass; pass0 += Grp::warps * NB) {
         int page[NB];
         bool ok[NB];
         uint4 raw[NB][CPL];
@@ -452,6 +461,45 @@ __device__ void score_pages_ffma(const Grp &grp, const SelectParams &p, int b, i
 
 // ------------------------------------------------------------ one unit
 
+// What every thread (and, in a cluster split, every CTA) of unit u = (b, h)
+// knows before scoring: its page count, its kept count, whether scores are
+// needed.  `report`: this thread reports the sequence's length and budget
+// errors (one thread per sequence does).
+struct UnitPlan {
+    int b, h, N, k;
+    bool need_scores;
+};
+
+__device__ __forceinline__ UnitPlan plan_unit(const SelectParams &p, int u, bool report) {
+    UnitPlan s;
+    s.b = u / p.Hkv;
+    s.h = u % p.Hkv;
+    const bool rep = report && s.h == 0;
+    const int L = valid_len(p.seq_lens[s.b], p.max_pages, p.P, rep ? p.status : nullptr);
+    s.N = (L + p.P - 1) / p.P;
+    s.k = kept_pages(s.N, p.budget[s.b], p.max_budget, p.status, rep);
+    s.need_scores = s.N > 0 && ((s.k < s.N) || (p.scores_out != nullptr));
+    return s;
+}
+
+// Scores of the unit's pages in 16-page tiles [t_begin, t_end) into sc[page]
+// (sc may point into another CTA's shared memory of the cluster).
+template <typename T, int D, bool MMA, int GMAX, class Grp>
+__device__ __forceinline__ void score_window(const Grp &grp, const SelectParams &p, const UnitPlan &s, float *sc,
+                                             int t_begin, int t_end) {
+    if constexpr (is_fp8<T>::value) {
+        score_pages_fp8_mma<D>(grp, p, s.b, s.h, s.N, sc, t_begin, t_end);
+    } else if constexpr (MMA) {
+        score_pages_mma<T, D>(grp, p, s.b, s.h, s.N, sc, t_begin, t_end);
+    } else {
+        score_pages_ffma<T, D, GMAX>(grp, p, s.b, s.h, s.N, sc, t_begin, t_end);
+    }
+}
+
+template <class Grp>
+__device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u, const UnitPlan &s, float *sc,
+                                   SelScratch &x);
+
 // Score and select unit u = (b, h) of the batch: writes its row of
 // p.selected (ascending ids, -1 padded) and, if requested, its scores.  sc
 // holds max_pages floats of shared memory (scores, then keys in place).
@@ -459,33 +507,35 @@ __device__ void score_pages_ffma(const Grp &grp, const SelectParams &p, int b, i
 template <typename T, int D, bool MMA, int GMAX, class Grp>
 __device__ void select_unit(const Grp &grp, const SelectParams &p, int u, float *sc, SelScratch &x,
                             const BoxStage *stage = nullptr, uint32_t *phase_bits = nullptr) {
+    const UnitPlan s = plan_unit(p, u, grp.tid == 0);
+    if (s.need_scores) {
+        if constexpr (MMA && !is_fp8<T>::value) {
+            if (stage) score_pages_mma_staged<T, D>(grp, p, s.b, s.h, s.N, sc, *stage, *phase_bits);
+            else score_window<T, D, MMA, GMAX>(grp, p, s, sc, 0, (s.N + 15) >> 4);
+        } else {
+            score_window<T, D, MMA, GMAX>(grp, p, s, sc, 0, (s.N + 15) >> 4);
+        }
+        grp.sync();
+    }
+    select_from_scores(grp, p, u, s, sc, x);
+}
+
+// The unit's selection once sc[0, N) holds its scores (when s.need_scores).
+template <class Grp>
+__device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u, const UnitPlan &s, float *sc,
+                                   SelScratch &x) {
     uint32_t *keys = reinterpret_cast<uint32_t *>(sc);
     constexpr int NT = Grp::warps * 32;
-    const int b = u / p.Hkv, h = u % p.Hkv;
     const int tid = grp.tid, lane = grp.lane();
-    const int L = valid_len(p.seq_lens[b], p.max_pages, p.P, (h == 0 && tid == 0) ? p.status : nullptr);
-    const int N = (L + p.P - 1) / p.P;
-    const int k = kept_pages(N, p.budget[b], p.max_budget, p.status, h == 0 && tid == 0);
+    const int N = s.N, k = s.k;
     int32_t *selrow = p.selected + (size_t)u * p.max_budget;
 
     if (N == 0) {
         for (int j = tid; j < p.max_budget; j += NT) selrow[j] = -1;
         return;
     }
-    const bool need_scores = (k < N) || (p.scores_out != nullptr);
-    if (need_scores) {
-        if constexpr (is_fp8<T>::value) {
-            score_pages_fp8_mma<D>(grp, p, b, h, N, sc);
-        } else if constexpr (MMA) {
-            if (stage) score_pages_mma_staged<T, D>(grp, p, b, h, N, sc, *stage, *phase_bits);
-            else score_pages_mma<T, D>(grp, p, b, h, N, sc);
-        } else {
-            score_pages_ffma<T, D, GMAX>(grp, p, b, h, N, sc);
-        }
-        grp.sync();
-        if (p.scores_out)
-            for (int i = tid; i < N; i += NT) p.scores_out[(size_t)u * p.max_pages + i] = sc[i];
-    }
+    if (s.need_scores && p.scores_out)
+        for (int i = tid; i < N; i += NT) p.scores_out[(size_t)u * p.max_pages + i] = sc[i];
     if (k >= N) {
         for (int j = tid; j < p.max_budget; j += NT) selrow[j] = j < N ? j : -1;
         return;
