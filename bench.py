@@ -339,10 +339,19 @@ def oracle_sample(cfg, seed, seconds=15.0, threads=None):
             break
     el = time.perf_counter() - t0
     qps = done / cfg.num_kv_heads / el
+    # the same units on one core, for a fifth of the time
+    done1 = 0
+    t1 = time.perf_counter()
+    while time.perf_counter() - t1 < seconds / 5:
+        one(units[done1 % len(units)])
+        done1 += 1
+    el1 = time.perf_counter() - t1
     return {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
             "sample": "%d (sequence, KV head) units of %s (%d sequences) repeated for %.1f s; "
                       "score+select+attend per unit, fp64, page boxes prebuilt"
-                      % (done, cfg.name, b, el)}
+                      % (done, cfg.name, b, el),
+            "single_thread": {"value": done1 / cfg.num_kv_heads / el1, "unit": "queries/s", "cores": 1,
+                              "sample": "%d units in %.1f s" % (done1, el1)}}
 
 
 def run_reference(args):
@@ -711,6 +720,7 @@ def run_ours(args):
         "unit": "queries/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_all,
+        "ms_per_step_median": max_over_ranks(statistics.median(step_ms), dev),
         "per_head_queries_per_s": world * B * Hq / (ms_all * 1e-3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic",
