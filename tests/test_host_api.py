@@ -102,3 +102,17 @@ def test_workspace_size_rejects_bad_shapes(lib):
     assert lib._lib.qasa_decode_workspace_size(-1, 32, ctypes.byref(c), 512) == 0
     assert lib._lib.qasa_decode_workspace_size(8, 2, ctypes.byref(c), 512) == 0
     assert lib._lib.qasa_decode_workspace_size(8, 32, None, 512) == 0
+
+
+def test_host_call_form_query(lib, monkeypatch):
+    # direct form only when all six buffers are page-locked memory the device
+    # addresses at the same pointer: a missing buffer, ordinary (pageable)
+    # host memory, or QASA_HOST_DIRECT=0 give the staged form (0)
+    f = lib._lib.qasa_host_call_is_direct
+    bufs = [ctypes.create_string_buffer(64) for _ in range(6)]
+    ptrs = [ctypes.addressof(b) for b in bufs]
+    for i in range(6):
+        assert f(*[None if j == i else p for j, p in enumerate(ptrs)]) == 0
+    assert f(*ptrs) == 0
+    monkeypatch.setenv("QASA_HOST_DIRECT", "0")
+    assert f(*ptrs) == 0
