@@ -201,3 +201,17 @@ def test_fp8_through_the_other_entry_points(monkeypatch):
     with pytest.raises(qasa.QasaError) as err:
         qasa.page_attention_mass(case.cache, case.q_dev, case.bt, case.lens_dev)
     assert "dtype" in str(err.value)
+
+
+def test_fp8_full_size_sampled_units():
+    # the benchmark's FP8 workload at full size (B = 128, 8K, 12.5 %), in its
+    # launch configuration: cache state and decode checked on sampled units
+    cfg = _fp8("headline_8k")
+    case = H.make_case(cfg, seed=0, poison=False)
+    units = _units(case)
+    rng = np.random.default_rng(0)
+    pick = [units[i] for i in rng.choice(len(units), size=6, replace=False)] + [units[0], units[-1]]
+    _check_cache(case, None, pick)
+    out, sel, scores = _decode(case)
+    _check_decode(case, None, pick, out, sel, scores)
+    assert torch.isfinite(out.float()).all()
