@@ -1,0 +1,187 @@
+"""CPU model of the attention kernel's work split, checked for every grid size
+the library launches (1 .. SM count; small batches get fewer CTAs than SMs).
+
+The kernel flattens all kept (unit, page) pairs unit-major (unit = sequence b,
+KV head h; sequence b contributes Hkv units of cnt_b pages each), gives CTA c of
+C the range [c*T/C, (c+1)*T/C), walks it rotated (first the part of its last
+unit that starts inside the range, then the rest), writes whole units directly
+and, for a unit cut by a range boundary, a partial to slot unit + c plus a page
+ticket; the CTA whose ticket completes the unit merges the partials of CTAs
+cta_of(first page) .. cta_of(last page).  The single-launch form also lets the
+CTA holding a unit's first page select that unit.  This model restates that
+index arithmetic (range_start, cta_of, locate, the rotation) and checks:
+
+* the segments of all CTAs tile [0, T) exactly, each inside one unit;
+* a CTA has at most one segment per unit, and a unit handled whole by one CTA
+  is written directly (no ticket, no slot);
+* partial slots unit + c are distinct and below U + C (the workspace holds
+  U + SM-count slots);
+* every split unit's tickets add up to its page count, so exactly one CTA
+  completes it, and the merge range is exactly the CTAs that wrote partials;
+* every unit with pages has exactly one selecting CTA, which holds its first
+  page;
+* the grid for small batches is at least 1 and at most the SM count.
+"""
+import random
+
+import pytest
+
+
+class Split:
+    def __init__(self, cnts, Hkv, C):
+        self.B, self.Hkv, self.C, self.cnts = len(cnts), Hkv, C, cnts
+        self.prefix = [0]
+        for x in cnts:
+            self.prefix.append(self.prefix[-1] + x)
+        self.T = Hkv * self.prefix[-1]
+
+    def range_start(self, c):
+        return c * self.T // self.C
+
+    def cta_of(self, g):
+        return ((g + 1) * self.C - 1) // self.T
+
+    def locate(self, g):
+        lo, hi = 0, self.B - 1
+        while lo < hi:   # largest b with Hkv * prefix[b] <= g
+            mid = (lo + hi + 1) >> 1
+            if self.Hkv * self.prefix[mid] <= g:
+                lo = mid
+            else:
+                hi = mid - 1
+        b = lo
+        cnt = self.prefix[b + 1] - self.prefix[b]
+        off = g - self.Hkv * self.prefix[b]
+        h = off // cnt
+        return b, h, self.Hkv * self.prefix[b] + h * cnt, cnt
+
+    def segments(self, c):
+        """(g, s1, unit, unit start, unit end) in the order CTA c walks them."""
+        g0, g1 = self.range_start(c), self.range_start(c + 1)
+        n_loc = g1 - g0
+        gL = g0
+        if n_loc > 0:
+            _, _, us, _ = self.locate(g1 - 1)
+            if us > g0:
+                gL = us
+        nL = g1 - gL
+
+        def rot(pos):
+            return gL + pos if pos < nL else g0 + (pos - nL)
+
+        def run_end(pos):
+            return g1 if pos < nL else gL
+
+        out, pos = [], 0
+        while pos < n_loc:
+            g = rot(pos)
+            b, h, us, cnt = self.locate(g)
+            ue = us + cnt
+            s1 = min(run_end(pos), ue)
+            out.append((g, s1, b * self.Hkv + h, us, ue))
+            pos += s1 - g
+        return out
+
+    def selected_units(self, c):
+        """Units the single-launch CTA c selects (its last unit first)."""
+        g0, g1 = self.range_start(c), self.range_start(c + 1)
+        if g1 <= g0:
+            return []
+        b, h, us, _ = self.locate(g1 - 1)
+        u_last = b * self.Hkv + h
+        sel = [u_last] if us >= g0 else []
+        b, h, us, _ = self.locate(g0)
+        u = b * self.Hkv + h + (1 if us < g0 else 0)
+        while u < u_last:
+            ub = u // self.Hkv
+            if self.prefix[ub + 1] != self.prefix[ub]:
+                sel.append(u)
+            u += 1
+        return sel
+
+
+def check(cnts, Hkv, C):
+    m = Split(cnts, Hkv, C)
+    if m.T == 0:
+        return
+    segs = []
+    partial_writers = {}          # unit -> CTAs that wrote a partial
+    ticket = {}                   # unit -> pages ticketed
+    slots = set()
+    for c in range(C):
+        seen = set()
+        for g, s1, u, us, ue in m.segments(c):
+            assert us <= g < s1 <= ue, (g, s1, us, ue)
+            assert m.range_start(c) <= g and s1 <= m.range_start(c + 1)
+            assert u not in seen, ("two segments of one unit in a CTA", u, c)
+            seen.add(u)
+            segs.append((g, s1))
+            if g == us and s1 == ue:
+                continue                              # whole unit: written directly
+            slot = u + c
+            assert slot not in slots and slot < m.B * Hkv + C, (slot, u, c)
+            slots.add(slot)
+            partial_writers.setdefault(u, set()).add(c)
+            ticket[u] = ticket.get(u, 0) + (s1 - g)
+    segs.sort()
+    assert segs[0][0] == 0 and segs[-1][1] == m.T
+    for (a0, a1), (b0, b1) in zip(segs, segs[1:]):
+        assert a1 == b0, "segments must tile the flattened pages"
+    for u, writers in partial_writers.items():
+        b = u // Hkv
+        cnt = cnts[b]
+        us = Hkv * m.prefix[b] + (u % Hkv) * cnt
+        assert ticket[u] == cnt                       # exactly one CTA completes it
+        merged = {x for x in range(m.cta_of(us), m.cta_of(us + cnt - 1) + 1)
+                  if m.range_start(x) != m.range_start(x + 1)}
+        assert merged == writers, (u, merged, writers)
+    owner = {}
+    for c in range(C):
+        for u in m.selected_units(c):
+            assert u not in owner, ("unit selected twice", u)
+            owner[u] = c
+    for u in range(m.B * Hkv):
+        b = u // Hkv
+        if cnts[b] == 0:
+            assert u not in owner
+            continue
+        us = Hkv * m.prefix[b] + (u % Hkv) * cnts[b]
+        assert m.range_start(owner[u]) <= us < m.range_start(owner[u] + 1)
+
+
+def attention_grid(units, most_pages_per_unit, sms, min_pages_per_cta=8):
+    """The host's grid: one CTA per SM, fewer when the batch's most pages give
+    fewer than min_pages_per_cta per CTA."""
+    want = -(-units * most_pages_per_unit // min_pages_per_cta)
+    return max(1, min(sms, want))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_work_split_invariants_for_every_grid(seed):
+    rng = random.Random(seed)
+    for _ in range(1500):
+        B = rng.randint(1, 24)
+        Hkv = rng.choice([1, 2, 4, 8])
+        cnts = [rng.choice([0, 1, 2, 3, 5, 6, 16, 64, 128, 200]) for _ in range(B)]
+        most = max(cnts) if max(cnts) else 2
+        C = rng.choice([1, 2, 3, 5, 8, 37, 64, 151, 152,
+                        attention_grid(B * Hkv, most, 152)])
+        check(cnts, Hkv, C)
+
+
+def test_headline_and_small_batch_shapes():
+    check([64] * 128, 4, 152)                       # the 8K / 12.5 % headline
+    check([16], 4, attention_grid(4, 16, 152))      # one sequence: 8 CTAs
+    check([64, 64], 4, attention_grid(8, 64, 152))  # two sequences: 64 CTAs
+    check([0, 40, 0, 3, 2, 128], 4, 152)            # empty sequences and ragged budgets
+
+
+def test_small_batch_grid_bounds():
+    assert attention_grid(4, 16, 152) == 8
+    assert attention_grid(512, 64, 152) == 152
+    assert attention_grid(1, 2, 152) == 1
+    for units in range(1, 60):
+        for most in (2, 3, 7, 8, 9, 64):
+            C = attention_grid(units, most, 152)
+            assert 1 <= C <= 152
+            assert C == 152 or units * most <= 8 * C
