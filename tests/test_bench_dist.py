@@ -3,6 +3,7 @@
 Every rank decodes its own batch (weak scaling): distinct seeds, no data-path
 collective; the only collective is the max over ranks of the step time.
 """
+import json
 import os
 import socket
 
@@ -75,3 +76,35 @@ def test_algorithmic_bytes_of_the_headline_case():
 def test_bench_rejects_short_warmup():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    # the reference arm is the oracle on the host cores: one JSON line with the
+    # arm's metric, config and unit, a cpu_baseline describing the run and an
+    # e2e with no host-device bytes (the oracle sample is replaced by a stub here)
+    calls = []
+
+    def stub(cfg, seed, seconds=15.0, threads=None):
+        calls.append((cfg.name, seed, seconds))
+        return {"value": 1234.5, "unit": "queries/s", "cores": 3, "kind": "oracle", "sample": "stub"}
+
+    monkeypatch.setattr(bench, "oracle_sample", stub)
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "4", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] == 1234.5 and line["unit"] == "queries/s" and line["higher_is_better"] is True
+    assert line["steps"] == 4 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["config"]["workload"] == "headline_8k"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == 1234.5
+    assert line["e2e"] == {"value": 1234.5, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert calls == [("headline_8k", 0, calls[0][2])] and calls[0][2] >= 2.0 * 7
+
+    # under torchrun only rank 0 runs and prints it
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--gpus", "2"]) == 0
+    assert capsys.readouterr().out.strip() == ""
+    assert len(calls) == 1
