@@ -1,8 +1,9 @@
 // select_device.cuh -- query-aware page scoring and top-k selection of ONE
 // (sequence, KV head), run by a group of NT threads.  Used by the standalone
-// selection kernel (the whole CTA is the group) and by the single-launch
-// decode kernel (four selector warps of a larger CTA, synchronised by a named
-// barrier).
+// selection kernel (the whole CTA is the group), by its cluster form (each CTA
+// of a cluster scores a window of the unit's tiles with score_window, the first
+// runs select_from_scores) and by the single-launch decode kernel (four
+// selector warps of a larger CTA, synchronised by a named barrier).
 //
 // "TinyServe: Query-Aware Cache Selection for Efficient LLM Serving",
 // 方法详解 / 关键设计: at decode time the query is compared with the bounding
