@@ -376,6 +376,39 @@ def test_e4m3_round_trip_saturation_and_zero():
     assert oracle.e4m3_encode(np.float32([-0.0, -1e-30, 1e30, -1e30, 449.0]))[:5].tolist() == [0, 0, 0x7E, 0xFE, 0x7E]
 
 
+def test_fp8_scale_closed_forms():
+    # scale = amax / 448 in fp32: exact for amax = 448 * 2^k, zero for a zero
+    # page, monotone in amax, and within half an fp32 ulp of the real quotient
+    k = np.arange(-20, 21)
+    amax = np.float32(448.0) * np.exp2(k).astype(np.float32)
+    assert np.array_equal(oracle.fp8_scale(amax), np.exp2(k).astype(np.float32))
+    assert oracle.fp8_scale(np.float32([0.0]))[0] == 0.0
+    a = np.sort(rng(43).random(2000).astype(np.float32) * 1000)
+    s = oracle.fp8_scale(a)
+    assert s.dtype == np.float32 and np.all(np.diff(s) >= 0)
+    exact = a.astype(np.float64) / 448.0
+    assert np.all(np.abs(s - exact) <= 0.5 * np.spacing(s.astype(np.float32)).astype(np.float64))
+
+
+def test_fp8_dequant_closed_forms():
+    # code * scale per row: 1.0 (0x38) and -1.0 (0xB8) give +-scale, the
+    # largest finite code (0x7E = 448) gives 448 * scale, zero gives 0; and a
+    # value quantized under its row's scale comes back within half a code step
+    sc = np.array([0.5, 3.0, 1e-3], dtype=np.float32)
+    codes = np.tile(np.uint8([0x38, 0xB8, 0x7E, 0x00]), (3, 1))
+    v = oracle.fp8_dequant(codes, sc)
+    assert v.dtype == np.float64
+    assert np.array_equal(v[:, 0], sc.astype(np.float64)) and np.array_equal(v[:, 1], -sc.astype(np.float64))
+    assert np.array_equal(v[:, 2], 448.0 * sc.astype(np.float64)) and not v[:, 3].any()
+    x = rng(44).standard_normal((3, 64)).astype(np.float32) * np.float32(100.0) * sc[:, None]
+    q = oracle.e4m3_encode(x / sc[:, None])
+    back = oracle.fp8_dequant(q, sc)
+    mag = np.abs(oracle.e4m3_decode(q)).astype(np.float64)
+    # E4M3 step at a value of magnitude m: 2^(floor(log2 m) - 3) (normals), 2^-9 below 2^-6
+    step = np.where(mag >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(mag, 2.0 ** -6))) - 3), 2.0 ** -9)
+    assert np.all(np.abs(back - x) <= 0.5 * step * sc[:, None] * (1 + 1e-6) + 1e-30)
+
+
 def _fp8_page_check(X, P, codes, amax, lo, hi):
     L, d = X.shape
     for p in range(-(-L // P)):
