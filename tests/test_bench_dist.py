@@ -108,3 +108,18 @@ def test_reference_arm_line(monkeypatch, capsys):
     assert bench.main(["--impl", "reference", "--gpus", "2"]) == 0
     assert capsys.readouterr().out.strip() == ""
     assert len(calls) == 1
+
+
+def test_kept_counts_follow_the_oracle_selection():
+    # the benchmark's byte model counts the pages the selection keeps; it must
+    # agree with the oracle's selection on the count for every length and budget
+    import oracle
+    rng = np.random.default_rng(5)
+    P = 16
+    lens = np.concatenate([[0, 1, 15, 16, 17, 32, 33], rng.integers(0, 4000, 60)])
+    budgets = np.concatenate([[1, 1, 2, 3, 1, 2, 40], rng.integers(1, 300, 60)])
+    k = bench.kept_counts(lens, budgets, P, 1 << 30)
+    for L, bud, kk in zip(lens, budgets, k):
+        N = oracle.num_pages(L, P)
+        scores = rng.standard_normal(N)
+        assert len(oracle.select_pages(scores, int(bud))) == kk, (L, bud)
