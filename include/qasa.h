@@ -258,8 +258,12 @@ qasa_status qasa_dense_decode_attention(const qasa_kv_cache *cache, const void *
  * serves instead, and nothing is allocated (no cudaMalloc, cudaFree or other
  * allocating routine).  A shape whose qasa_decode_workspace_size exceeds that
  * size is rejected with QASA_ERR_WORKSPACE before any launch.
- *   - The first call on a device (that device current) looks up the buffer's
- *     device address once; make that first call before any stream capture.
+ *   - Every call made outside stream capture looks up the buffer's device
+ *     address on the current device (so a context re-created after
+ *     cudaDeviceReset is followed); a call made while the stream is being
+ *     captured reuses the last address seen on that device, so make the
+ *     first call on a device before any stream capture, and make one more
+ *     call outside capture after a cudaDeviceReset before capturing again.
  *   - All calls on a device share the buffer, which keeps the last call's
  *     contents; what must start at zero is cleared inside each call.  Calls
  *     that overlap on the GPU (other streams) race: serialise them.

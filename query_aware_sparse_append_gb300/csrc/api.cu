@@ -18,6 +18,17 @@ constexpr int kMaxPagesPerSeq = 16384;
 constexpr int kMaxBatch = 8192;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
+// Limit of the waits on other warps, CTAs and flags.  QASA_WAIT_LIMIT_NS
+// (diagnostic, for tests of the time-out path) shortens it, down to 1 us; the
+// waits for a CTA's own copies in flight always keep kWaitLimitNs.
+unsigned long long wait_limit_ns() {
+    const char *v = std::getenv("QASA_WAIT_LIMIT_NS");
+    if (!v) return kWaitLimitNs;
+    const unsigned long long n = std::strtoull(v, nullptr, 10);
+    if (n < 1000ull) return 1000ull;
+    return n < kWaitLimitNs ? n : kWaitLimitNs;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t elem_size(qasa_dtype dt) { return dt == QASA_DTYPE_F32 ? 4 : dt == QASA_DTYPE_E4M3 ? 1 : 2; }
@@ -313,7 +324,8 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     p.one_box = one_box;
     p.stages = 0;
     p.consumers = 0;
-    p.wait_limit_ns = kWaitLimitNs;
+    p.wait_limit_ns = wait_limit_ns();
+    p.drain_limit_ns = kWaitLimitNs;
     p.bounds = cache->page_bounds;
     p.scores_out = scores_out;
     p.ready = reinterpret_cast<int32_t *>(ws + w.counters) + units;

@@ -35,6 +35,9 @@
 //
 // Every wait is bounded: a wait that gives up sets QASA_DEVERR_TIMEOUT, the CTA
 // stops issuing, drains the copies it issued (again bounded) and returns.
+// Waits on other warps, other CTAs or flags use p.wait_limit_ns; waits for the
+// CTA's own copies in flight use p.drain_limit_ns, so that no CTA exits while
+// a copy into its shared memory can still land.
 #include <cstdlib>
 #include <type_traits>
 
@@ -300,7 +303,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             stage.bar = sel_bar;
             stage.phys = sel_phys;
             stage.slots_per_warp = kSelSlotsPerWarp;
-            stage.wait_limit_ns = p.wait_limit_ns;
+            stage.wait_limit_ns = p.drain_limit_ns;   // bulk copies of this CTA: drained, never abandoned
             uint32_t phase_bits = 0;    // parity of this warp's staging slots
             auto run_unit = [&](int u) {
                 select_unit<T, D, MMA, GMAX>(grp, sp, u, sel_sc, *sel_x, MMA ? &stage : nullptr, &phase_bits);
@@ -506,7 +509,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         __syncwarp();
         for (int s = lane; s < S; s += 32) {
             const int ph = last_ph[s];
-            if (ph >= 0 && !mbar_wait_bounded(&full_bar[s], (uint32_t)ph, p.wait_limit_ns) && p.status)
+            if (ph >= 0 && !mbar_wait_bounded(&full_bar[s], (uint32_t)ph, p.drain_limit_ns) && p.status)
                 atomicOr(p.status, QASA_DEVERR_TIMEOUT);
         }
         return;

@@ -11,9 +11,11 @@
 // Properties of the buffer (all stated in include/qasa.h):
 //   - QASA_NOALLOC_SCRATCH_BYTES bytes, a file-scope __device__ array: every
 //     device that loads the library holds it until the process exits;
-//   - its device address is looked up once per device, on the first call made
-//     with that device current (cudaGetSymbolAddress); that first call should
-//     come before any stream capture;
+//   - its device address is looked up with cudaGetSymbolAddress on every call
+//     made outside stream capture (so a context torn down and re-created, e.g.
+//     after cudaDeviceReset, is followed), and the last address seen per
+//     device is reused while the stream is being captured; the first call on
+//     a device should therefore come before any stream capture;
 //   - every call on a device shares it and it keeps the last call's contents;
 //     the parts that must start at zero (the tickets) are cleared by the
 //     selection kernel of each call; calls that overlap on the GPU race.
@@ -29,16 +31,21 @@ constexpr int kMaxDevices = 64;
 std::mutex g_lock;
 void *g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch buffer for the current device (looked up once).
-qasa_status scratch_for_current_device(void **ptr) {
+// Device address of the scratch buffer for the current device: looked up
+// again on every call made outside stream capture; during a capture the last
+// address seen on this device is used (none yet: an error).
+qasa_status scratch_for_current_device(cudaStream_t stream, void **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QASA_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return QASA_ERR_CUDA;
     std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_scratch[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, qasa_noalloc_scratch) != cudaSuccess || !p) return QASA_ERR_CUDA;
         g_scratch[dev] = p;
     }
+    if (!g_scratch[dev]) return QASA_ERR_CUDA;
     *ptr = g_scratch[dev];
     return QASA_OK;
 }
@@ -54,7 +61,7 @@ extern "C" qasa_status qasa_sparse_decode_attention_noalloc(
     if (batch > 0 && need == 0) return cache ? QASA_ERR_SHAPE : QASA_ERR_NULL;
     if (need > (size_t)QASA_NOALLOC_SCRATCH_BYTES) return QASA_ERR_WORKSPACE;   // beyond the fixed buffer
     void *scratch = nullptr;
-    const qasa_status st = scratch_for_current_device(&scratch);
+    const qasa_status st = scratch_for_current_device(stream, &scratch);
     if (st != QASA_OK) return st;
     return qasa_sparse_decode_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens,
                                         budget_pages, max_budget, scale, out, selected, scores_out, scratch,

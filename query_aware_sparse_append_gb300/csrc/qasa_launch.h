@@ -56,7 +56,8 @@ struct AttnParams {
                        // 1: one 3-D TMA box per K/V tile; 0: one 2-D box per 128 bytes of head dim
     int stages;        // ring depth, a multiple of `consumers`
     int consumers;     // consumer warps that take pages (<= the compiled count)
-    unsigned long long wait_limit_ns;
+    unsigned long long wait_limit_ns;    // waits on other warps, CTAs or flags
+    unsigned long long drain_limit_ns;   // waits for this CTA's own copies in flight (never shortened)
     // single-launch decode only: the selection inputs and outputs
     const void *bounds;
     float *scores_out;

@@ -3,9 +3,11 @@
 Element-by-element at reduced batch (several tiles, ragged tails); sampled
 (sequence, KV head) units at the full sizes the benchmark runs.  Bars:
 page boxes exact; scores within the fp32 summation bound; kept page sets
-identical wherever the boundary scores are not tied (1e-5 relative, widened
-to the fp32 bound); outputs within 2e-3 absolute + 1e-2 relative of the fp64
-oracle (on the GPU's own selection when a tie let the sets differ).
+identical unless the pages that differ have oracle scores within 1e-5
+relative of each other, or within the fp32 summation bounds of those two
+pages (counted and reported at the end of the session); outputs within
+2e-3 absolute + 1e-2 relative of the fp64 oracle (on the GPU's own selection
+when a tie let the sets differ).
 """
 import numpy as np
 import pytest
@@ -47,47 +49,8 @@ def run_sparse(case, max_budget=None, budget=None):
     return out, sel, scores, int(status.item())
 
 
-def check_units(case, out, sel, scores, units, check_bounds=True):
-    cfg = case.cfg
-    P = cfg.page_size
-    out64 = H.gpu_out64(out, cfg.dtype)
-    sel = sel.cpu().numpy()
-    scores = scores.cpu().numpy()
-    bounds = H.from_torch(case.cache.page_bounds, cfg.dtype) if check_bounds else None
-    n_equal = 0
-    for b, h in units:
-        L = int(case.lens[b])
-        N = -(-L // P)
-        K = case.k64(b, h)
-        lo, hi = oracle.page_bounds(K, P)
-        if check_bounds and N:
-            phys = case.plan.block_table[b, :N]
-            glo = W.widen(bounds[phys, h, 0], cfg.dtype)
-            ghi = W.widen(bounds[phys, h, 1], cfg.dtype)
-            assert np.array_equal(glo, lo) and np.array_equal(ghi, hi), (b, h)
-        q64 = case.q64(b, h)
-        o_s, o_sel, o_out = oracle.decode_unit(q64, K, case.v64(b, h), lo, hi, L, P,
-                                               int(case.budgets[b]))
-        if N == 0:
-            assert np.all(sel[b, h] == -1)
-            assert np.all(out64[b, h * case.G:(h + 1) * case.G] == 0)
-            continue
-        g_s = scores[b, h, :N].astype(np.float64)
-        k_eff = len(o_sel)
-        if k_eff < N:
-            tol = H.score_tolerance(q64, lo, hi)
-            assert np.all(np.abs(g_s - o_s) <= tol), (b, h, np.max(np.abs(g_s - o_s) - tol))
-        same = H.check_selection(sel[b, h], g_s if k_eff < N else None, o_s, o_sel, k_eff,
-                                 H.score_tolerance(q64, lo, hi))
-        ref = o_out if same else oracle.attention(q64, K, case.v64(b, h), L, P,
-                                                  sel[b, h][sel[b, h] >= 0])
-        n_equal += same
-        H.assert_close(out64[b, h * case.G:(h + 1) * case.G], ref, "out b=%d h=%d" % (b, h))
-    return n_equal
-
-
-def all_units(case):
-    return [(b, h) for b in range(case.cfg.batch) for h in range(case.cfg.num_kv_heads)]
+check_units = H.check_units
+all_units = H.all_units
 
 
 # ------------------------------------------------------------- reduced sizes

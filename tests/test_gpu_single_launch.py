@@ -5,8 +5,9 @@ cooperative persistent kernel; with QASA_SINGLE_LAUNCH=0 it runs the selection
 kernel and then the attention kernel.  Both use the same scoring and selection
 code, so kept ids and scores must agree bit for bit; the attention outputs may
 differ in summation order (a different number of consumer warps) and must
-agree within the output tolerance, and each must match the oracle (the other
-GPU tests check the one-launch form against the oracle on many more cases).
+agree within the output tolerance.  The one-launch form has its own selector
+code path (selector warps, bulk-copy box staging, ready flags), so its kept
+ids, scores and outputs are also checked against the oracle at every unit.
 """
 import os
 
@@ -14,7 +15,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 from query_aware_sparse_append_gb300 import workloads as W
 from tests import harness as H
 
@@ -68,16 +68,9 @@ def test_one_launch_equals_two_launches(name, batch, seed):
     for b in range(case.cfg.batch):
         assert torch.equal(c1[b, :, :N[b]], c2[b, :, :N[b]])
     H.assert_close(H.gpu_out64(o1, case.cfg.dtype), H.gpu_out64(o2, case.cfg.dtype), "one vs two launches")
-    # and the one-launch result against the oracle on a few units
-    P = case.cfg.page_size
-    out64, sel = H.gpu_out64(o1, case.cfg.dtype), s1.cpu().numpy()
-    units = [(0, 0), (case.cfg.batch - 1, case.cfg.num_kv_heads - 1)]
-    for b, h in units:
-        L = int(case.lens[b])
-        K = case.k64(b, h)
-        kept = sel[b, h][sel[b, h] >= 0]
-        ref = oracle.attention(case.q64(b, h), K, case.v64(b, h), L, P, kept)
-        H.assert_close(out64[b, h * case.G:(h + 1) * case.G], ref, "b=%d h=%d" % (b, h))
+    # the one-launch result against the oracle at every unit: kept sets (tie
+    # rule), scores (fp32 bound) and outputs
+    H.check_units(case, o1, s1, c1, H.all_units(case))
 
 
 def test_one_launch_with_empty_sequences_and_full_budgets():
@@ -92,6 +85,7 @@ def test_one_launch_with_empty_sequences_and_full_budgets():
     g = H.gpu_out64(o1, cfg.dtype)
     assert np.all(g[0] == 0) and np.all(g[3] == 0)
     H.assert_close(g, H.gpu_out64(o2, cfg.dtype), "one vs two launches")
+    H.check_units(case, o1, s1, None, H.all_units(case))
 
 
 def test_one_launch_repeated_calls_reuse_the_workspace():
@@ -111,3 +105,4 @@ def test_one_launch_repeated_calls_reuse_the_workspace():
     for out, sel in outs[1:]:
         assert torch.equal(sel, outs[0][1])
         assert torch.equal(out.view(torch.int16), outs[0][0].view(torch.int16))
+    H.check_units(case, outs[-1][0], outs[-1][1], None, H.all_units(case), check_bounds=False)

@@ -5,7 +5,8 @@ memory (a host framework owns all of it, or a device-synchronising cudaMalloc
 is not allowed where they run): it runs the decode step with the library's
 fixed device buffer instead of a caller workspace.  These tests call it through
 the C ABI and compare it with qasa_sparse_decode_attention on the same inputs,
-twice in a row (the buffer is shared and keeps the previous call's contents).
+twice in a row (the buffer is shared and keeps the previous call's contents),
+and each call's result with the CPU oracle.
 This file is collected last on purpose: it must pass on its own in a fresh
 process and after every other test.
 """
@@ -48,6 +49,8 @@ def test_noalloc_matches_the_workspace_entry_point_twice(name, batch, seed):
         assert int(status.item()) == 0
         assert torch.equal(sel, ref_sel), "call %d: kept pages differ" % call
         H.assert_close(H.gpu_out64(out, case.cfg.dtype), ref, "no-alloc call %d" % call)
+        # and against the oracle at every unit (kept sets under the tie rule, outputs)
+        H.check_units(case, out, sel, None, H.all_units(case), check_bounds=False)
 
 
 def test_noalloc_rejects_shapes_beyond_its_buffer():
