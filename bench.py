@@ -306,7 +306,7 @@ def oracle_sample(cfg, seed, seconds=15.0, threads=None):
     units = []
     b = 0
     t_prep = time.time()
-    while b < cfg.batch and (len(units) < 4 * threads or time.time() - t_prep < 5):
+    while b < cfg.batch and (len(units) < 4 * threads or time.time() - t_prep < min(5.0, seconds / 3)):
         s = W.sequence(cfg, b, int(lens[b]), seed, scales)
         for h in range(cfg.num_kv_heads):
             K = W.widen(s.k[:, h], cfg.dtype)
@@ -370,14 +370,17 @@ def run_reference(args):
             "ms_per_step": 1000.0 * cfg.batch / v, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_block(cfg), "cpu_baseline": base,
+            "ms_per_step_method": "batch / the sampled rate: the oracle decodes (sequence, KV head) units "
+                                  "of this workload for about (steps + warmup) * %.1f s; no per-step timing"
+                                  % per_step,
             "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def config_block(cfg, step_bytes=None):
-    mb = "%.0f MB" % (step_bytes / 1e6) if step_bytes else "the step's bytes"
+def config_block(cfg):
+    """The workload as both arms describe it (identical keys and values)."""
     return {"workload": cfg.name, "batch": cfg.batch, "ctx": [cfg.ctx_min, cfg.ctx_max],
             "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
             "head_dim": cfg.head_dim, "page_size": cfg.page_size,
@@ -385,7 +388,7 @@ def config_block(cfg, step_bytes=None):
                        if cfg.budget_kind == "permille" else "%d pages" % cfg.budget_value),
             "kv_dtype": cfg.dtype, "physical_pages": "shuffled",
             "l2": "between timed steps a 256 MB write evicts L2, then a 512 MB read leaves it "
-                  "clean; per-step bytes (%s) also exceed L2" % mb}
+                  "clean; the step's bytes also exceed L2"}
 
 
 # ------------------------------------------------------------ GPU leg
@@ -458,6 +461,177 @@ def run_hit_rate_table(args):
         del wl
         torch.cuda.empty_cache()
     return 0
+
+
+def trace_summary(buf, qasa, sel_ctas, att_ctas, raw=False):
+    """Percentiles (us, from the earliest recorded stamp) of every trace event
+    over the CTAs that recorded it."""
+    import numpy as np
+    t = buf.cpu().numpy().astype(np.int64)
+    nsel = qasa.TRACE_MAX_CTAS * qasa.TRACE_SELECT_EVENTS
+    sel = t[:nsel].reshape(qasa.TRACE_MAX_CTAS, qasa.TRACE_SELECT_EVENTS)[:sel_ctas]
+    att = t[nsel:].reshape(qasa.TRACE_MAX_CTAS, qasa.TRACE_ATTN_EVENTS)[:att_ctas]
+    ts, ta = sel[:, :3], att[:, :8]          # time stamps (the other columns hold SM ids)
+    rec = np.concatenate([ts[ts > 0], ta[ta > 0]])
+    if rec.size == 0:
+        return {}
+    t0 = rec.min()
+    names_s = ["start", "scored", "ids_written"]
+    names_a = ["start", "prologue_done", "dependency_wait_done", "first_copy_issued", "first_page_consumed",
+               "last_copy_issued", "consumers_done", "combiner_done"]
+    out = {}
+    for pre, arr, names in (("select.", sel, names_s), ("attn.", att, names_a)):
+        for j, nm in enumerate(names):
+            v = arr[:, j]
+            v = v[v > 0]
+            if v.size:
+                q = np.percentile((v - t0) / 1000.0, [0, 50, 100])
+                out[pre + nm] = [round(float(x), 2) for x in q]
+    if raw:
+        # per CTA, in launch order: every event (us from t0, null when not reached) and its SM
+        def us(a):
+            return [round(float((x - t0) / 1000.0), 2) if x > 0 else None for x in a]
+        out["raw"] = {"select_sm": sel[:, 3].tolist(), "attn_sm": att[:, 8].tolist()}
+        for pre, arr, names in (("select.", sel, names_s), ("attn.", att, names_a)):
+            for j, nm in enumerate(names):
+                out["raw"][pre + nm] = us(arr[:, j])
+    return out
+
+
+def run_trace(args):
+    """Per-CTA timelines of the decode step's kernels (globaltimer stamps),
+    one JSON line per repetition: [min, median, max] over CTAs, in us from the
+    first recorded stamp of the step."""
+    import torch
+    from query_aware_sparse_append_gb300 import build
+    build.build()
+    from query_aware_sparse_append_gb300 import binding as qasa
+    from query_aware_sparse_append_gb300 import paged
+    from query_aware_sparse_append_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    if args.batch:
+        cfg = cfg.with_batch(args.batch)
+    wl = paged.load(paged.generate(cfg, seed=args.seed), device=dev)
+    B, Hq, Hkv = cfg.batch, cfg.num_q_heads, cfg.num_kv_heads
+    maxp = wl.block_table.shape[1]
+    ws = qasa.alloc_workspace(wl.cache, B, Hq, maxp, device=dev)
+    out = torch.empty_like(wl.q_dev)
+    sel = torch.empty((B, Hkv, wl.max_budget), dtype=torch.int32, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_CLEAN_BYTES // 4, dtype=torch.int32, device=dev)
+    buf = torch.zeros(qasa.debug_trace_bytes() // 8, dtype=torch.int64, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def step():
+        qasa.sparse_decode_attention(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev, wl.budget_dev,
+                                     max_budget=wl.max_budget, out=out, selected=sel, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    for rep in range(args.steps):
+        flush_w.zero_()
+        flush_r.sum()
+        buf.zero_()
+        torch.cuda.synchronize(dev)
+        qasa.debug_trace(buf)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b_.record()
+        torch.cuda.synchronize(dev)
+        qasa.debug_trace(None)
+        line = {"trace": cfg.name, "rep": rep, "step_us": a.elapsed_time(b_) * 1000.0,
+                "form": "one launch" if os.environ.get("QASA_SINGLE_LAUNCH") == "1" else "two launches",
+                **trace_summary(buf, qasa, min(2 * sms, qasa.TRACE_MAX_CTAS), sms, raw=args.trace_raw)}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_steps(fn, steps, flush, stream):
+    """Mean CUDA-event time (ms) of `steps` calls of fn, L2 flushed before each."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b_ in ev:
+        flush()
+        a.record(stream)
+        fn()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b_) for a, b_ in ev)
+
+
+def measure_per_config(args, qasa, paged, W, dev, seed, status, with_cpu):
+    """The decode step (two launches) and the dense path on the other
+    workloads, and on the serving mix at every budget of its sweep: time per
+    step, queries/s, algorithmic bytes and their fraction of the measured HBM
+    peak, next to the oracle's queries/s on a bounded sample."""
+    import numpy as np
+    import torch
+    peak, _ = measured_peak()
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_CLEAN_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(5, args.steps // 2)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
+
+    def entry(wcfg, wl, lens, bud, label):
+        maxp = wl.block_table.shape[1]
+        bud = np.asarray(bud, dtype=np.int32)
+        mb = max(2, int(kept_counts(lens, bud, wcfg.page_size, 1 << 30).max()))
+        bud_dev = torch.from_numpy(bud).to(dev)
+        ws = qasa.alloc_workspace(wl.cache, wcfg.batch, wcfg.num_q_heads, maxp, device=dev)
+        out = torch.empty_like(wl.q_dev)
+        sel = torch.empty((wcfg.batch, wcfg.num_kv_heads, mb), dtype=torch.int32, device=dev)
+
+        def step():
+            qasa.sparse_decode_attention(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev, bud_dev,
+                                         max_budget=mb, out=out, selected=sel, workspace=ws, status=status)
+
+        def dense():
+            qasa.dense_decode_attention(wl.cache, wl.q_dev, wl.block_table, wl.lens_dev, out=out,
+                                        workspace=ws, status=status)
+
+        for _ in range(3):
+            step()
+            dense()
+        ms = time_steps(step, steps, flush, stream)
+        dms = time_steps(dense, max(3, steps // 2), flush, stream)
+        sb, ab, db = algorithmic_bytes(wcfg, lens, bud)
+        e = {"workload": label, "batch": wcfg.batch, "kv_dtype": wcfg.dtype,
+             "us_per_step": 1000.0 * ms, "queries_per_s": wcfg.batch / (ms * 1e-3),
+             "algorithmic_bytes": sb + ab, "achieved_gbs": (sb + ab) / (ms * 1e-3) / 1e9,
+             "frac_of_peak": (sb + ab) / (ms * 1e-3) / 1e9 / peak,
+             "kept_fraction": float(kept_counts(lens, bud, wcfg.page_size, 1 << 30).sum() /
+                                    max(1, W.num_pages(lens, wcfg.page_size).sum())),
+             "dense": {"us_per_step": 1000.0 * dms, "queries_per_s": wcfg.batch / (dms * 1e-3),
+                       "algorithmic_bytes": db, "frac_of_peak": db / (dms * 1e-3) / 1e9 / peak}}
+        if with_cpu and args.cpu_seconds > 0:
+            c = oracle_sample(wcfg, seed, seconds=max(1.0, args.cpu_seconds / 10))
+            e["oracle"] = {"queries_per_s": c["value"], "cores": c["cores"], "sample": c["sample"]}
+        return e
+
+    out = {}
+    for name in ("tiny", "tinyllama", "gpt2_345m", "llama_1b3_32k"):
+        wcfg = W.CONFIGS[name]
+        wl = paged.load(paged.generate(wcfg, seed=seed), device=dev)
+        out[name] = entry(wcfg, wl, wl.lens, wl.budgets, name)
+        del wl
+        torch.cuda.empty_cache()
+    mcfg = W.CONFIGS["serving_mix"]
+    wl = paged.load(paged.generate(mcfg, seed=seed), device=dev)
+    for pm in W.SERVING_MIX_BUDGETS_PERMILLE:
+        bcfg = mcfg.with_budget("permille", pm)
+        bud = W.budgets(bcfg, wl.lens)
+        out["serving_mix@%d" % pm] = entry(bcfg, wl, wl.lens, bud,
+                                           "serving_mix (ragged 512..16384, %g %% budget)" % (pm / 10.0))
+    del wl
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -670,41 +844,14 @@ def run_ours(args):
     h2d = sum(x.numel() * x.element_size() for x in (q_h, lens_h, bud_h, bt_h))
     d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
 
-    # ---- the ragged serving mix at a 12.5 % budget, reported next to the headline
-    mix = None
-    if args.serving_mix and cfg.name == "headline_8k":
-        mcfg = W.CONFIGS["serving_mix"].with_budget("permille", 125)
+    # ---- every other workload of the method's configurations, and the serving
+    # mix at each budget of its sweep, reported next to the headline (each a
+    # short timed loop; the oracle on a bounded sample of the same workload)
+    per_config = None
+    if args.per_config and cfg.name == "headline_8k":
         del ws, flush_w, flush_r
         torch.cuda.empty_cache()
-        mwl = paged.load(paged.generate(mcfg, seed=seed), device=dev)
-        mmb = mwl.max_budget
-        mws = qasa.alloc_workspace(mwl.cache, mcfg.batch, mcfg.num_q_heads, mwl.block_table.shape[1], device=dev)
-        mout = torch.empty_like(mwl.q_dev)
-        msel = torch.empty((mcfg.batch, mcfg.num_kv_heads, mmb), dtype=torch.int32, device=dev)
-        flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        flush_r = torch.zeros(L2_CLEAN_BYTES // 4, dtype=torch.int32, device=dev)
-
-        def mstep():
-            qasa.sparse_decode_attention(mwl.cache, mwl.q_dev, mwl.block_table, mwl.lens_dev, mwl.budget_dev,
-                                         max_budget=mmb, out=mout, selected=msel, workspace=mws, status=status)
-
-        for _ in range(3):
-            mstep()
-        evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for a, b_ in evm:
-            flush_w.zero_()
-            flush_r.sum()
-            a.record(stream)
-            mstep()
-            b_.record(stream)
-        torch.cuda.synchronize(dev)
-        mms = statistics.mean(a.elapsed_time(b_) for a, b_ in evm)
-        msb, mab, _ = algorithmic_bytes(mcfg, mwl.lens, mwl.budgets)
-        mix = {"workload": "serving_mix (ragged 512..16384, 12.5 % budget)", "batch": mcfg.batch,
-               "ms_per_step": mms, "queries_per_s": mcfg.batch / (mms * 1e-3),
-               "step_algorithmic_bytes": msb + mab,
-               "step_frac": (msb + mab) / (mms * 1e-3) / 1e9 / measured_peak()[0]}
+        per_config = measure_per_config(args, qasa, paged, W, dev, seed, status, rank == 0)
 
     if rank != 0:
         return 0
@@ -724,7 +871,7 @@ def run_ours(args):
         "per_head_queries_per_s": world * B * Hq / (ms_all * 1e-3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic",
-        "config": config_block(cfg, sel_b + att_b),
+        "config": config_block(cfg),
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (sparse attention over kept pages)",
                      "achieved": att_gbs, "peak": peak, "unit": "GB/s",
                      "frac": att_gbs / peak, "traffic": profiled_traffic(cfg.name),
@@ -744,7 +891,8 @@ def run_ours(args):
                   "frac": dense_b / (dense_ms * 1e-3) / 1e9 / peak,
                   "speedup_sparse_over_dense": dense_ms / ms},
         "page_hit_rate": hit,
-        "serving_mix": mix,
+        "serving_mix": (per_config or {}).get("serving_mix@125"),
+        "per_config": per_config,
         "metadata_rebuild": {"ms": rebuild_ms, "bytes": rebuild_b,
                              "achieved_gbs": rebuild_b / (rebuild_ms * 1e-3) / 1e9,
                              "frac": rebuild_b / (rebuild_ms * 1e-3) / 1e9 / peak},
@@ -769,10 +917,14 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-serving-mix", dest="serving_mix", action="store_false",
-                    help="skip the serving-mix measurement reported beside the headline")
+    ap.add_argument("--no-per-config", "--no-serving-mix", dest="per_config", action="store_false",
+                    help="skip the other workloads and the serving-mix budget sweep reported beside the headline")
     ap.add_argument("--hit-rate-table", action="store_true",
                     help="print the page hit rate per workload (--config all) and budget, then exit")
+    ap.add_argument("--trace", action="store_true",
+                    help="print per-CTA kernel timelines of the decode step (diagnostics), then exit")
+    ap.add_argument("--trace-raw", action="store_true",
+                    help="with --trace: also print every CTA's events and SM")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline (0 to skip)")
     args = ap.parse_args(argv)
@@ -782,6 +934,8 @@ def main(argv=None):
         return run_reference(args)
     if args.hit_rate_table:
         return run_hit_rate_table(args)
+    if args.trace:
+        return run_trace(args)
     return run_ours(args)
 
 

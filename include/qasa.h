@@ -358,6 +358,37 @@ int32_t qasa_host_call_is_direct(const void *q_host, const int32_t *block_table_
                                  const int32_t *seq_lens_host, const int32_t *budget_pages_host,
                                  const void *out_host, const int32_t *selected_host);
 
+/*
+ * Diagnostics (the paper has no counterpart): per-CTA timestamps of the
+ * decode-step kernels, for reading a step's timeline (when each CTA started,
+ * finished scoring, waited for the selection, issued its first copy, ...).
+ *
+ * qasa_debug_trace(buffer, bytes): every later launch of the selection and
+ * attention kernels in this process records %globaltimer values (ns) into
+ * `buffer` (device memory, 8-byte aligned, at least qasa_debug_trace_bytes()
+ * bytes, zeroed by the caller: a slot that stays 0 was not reached).  NULL
+ * turns recording off.  Process-wide and not thread-safe; a launch captured
+ * in a CUDA graph keeps the pointer it was captured with.  Returns
+ * QASA_ERR_WORKSPACE when `bytes` is too small, QASA_ERR_ALIGN when the
+ * buffer is misaligned.
+ *
+ * Layout (uint64): QASA_TRACE_MAX_CTAS rows of QASA_TRACE_SELECT_EVENTS for
+ * the selection kernel's CTAs, then QASA_TRACE_MAX_CTAS rows of
+ * QASA_TRACE_ATTN_EVENTS for the attention kernel's CTAs (CTAs beyond
+ * QASA_TRACE_MAX_CTAS record nothing).  Selection events: 0 CTA start,
+ * 1 the CTA's last tile scored, 2 the CTA's last warp done (selections
+ * included), 3 the SM the CTA ran on (an index, not a time).  Attention
+ * events: 0 CTA start, 1 prologue done, 2 wait for the preceding kernel done,
+ * 3 first page copy issued, 4 first page consumed, 5 last page copy issued,
+ * 6 last consumer warp done, 7 combiner done, 8 the SM the CTA ran on,
+ * 9 unused.
+ */
+#define QASA_TRACE_MAX_CTAS 4096
+#define QASA_TRACE_SELECT_EVENTS 4
+#define QASA_TRACE_ATTN_EVENTS 10
+size_t qasa_debug_trace_bytes(void);
+qasa_status qasa_debug_trace(unsigned long long *buffer, size_t bytes);
+
 /* Static description of a status code. */
 const char *qasa_status_string(qasa_status status);
 

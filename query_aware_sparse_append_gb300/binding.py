@@ -79,13 +79,22 @@ _lib.qasa_host_call_is_direct.restype = _I
 _lib.qasa_status_string.argtypes = [_I]
 _lib.qasa_status_string.restype = ctypes.c_char_p
 _lib.qasa_version.restype = _I
+_lib.qasa_debug_trace_bytes.restype = ctypes.c_size_t
+_lib.qasa_debug_trace.argtypes = [_P, ctypes.c_size_t]
+_lib.qasa_debug_trace.restype = _I
 
 EXPORTED = ("qasa_kv_append", "qasa_decode_workspace_size", "qasa_select_pages",
             "qasa_sparse_attention", "qasa_sparse_decode_attention",
             "qasa_dense_decode_attention", "qasa_sparse_decode_attention_noalloc",
             "qasa_rebuild_page_bounds", "qasa_page_attention_mass", "qasa_page_hit_rate",
             "qasa_host_decode_workspace_size", "qasa_sparse_decode_attention_host",
-            "qasa_host_call_is_direct", "qasa_status_string", "qasa_version")
+            "qasa_host_call_is_direct", "qasa_status_string", "qasa_version",
+            "qasa_debug_trace_bytes", "qasa_debug_trace")
+
+# trace buffer layout (include/qasa.h)
+TRACE_MAX_CTAS = 4096
+TRACE_SELECT_EVENTS = 4
+TRACE_ATTN_EVENTS = 10
 
 
 class QasaError(RuntimeError):
@@ -98,6 +107,20 @@ def library_path() -> str:
 
 def version() -> int:
     return int(_lib.qasa_version())
+
+
+def debug_trace(buffer: Optional[torch.Tensor]) -> None:
+    """Record per-CTA timestamps of every later selection and attention launch
+    into `buffer` (a zeroed int64 device tensor of at least
+    debug_trace_bytes() bytes); None turns recording off."""
+    if buffer is None:
+        _check(_lib.qasa_debug_trace(None, 0), "qasa_debug_trace")
+        return
+    _check(_lib.qasa_debug_trace(_ptr(buffer), buffer.numel() * buffer.element_size()), "qasa_debug_trace")
+
+
+def debug_trace_bytes() -> int:
+    return int(_lib.qasa_debug_trace_bytes())
 
 
 def status_string(code: int) -> str:

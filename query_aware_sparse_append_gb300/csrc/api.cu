@@ -90,6 +90,14 @@ size_t smem_optin() { return (size_t)device_attr(g_smem_optin, cudaDevAttrMaxSha
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Diagnostics: the trace buffer set by qasa_debug_trace (NULL: off).
+unsigned long long *g_trace = nullptr;
+
+unsigned long long *select_trace() { return g_trace; }
+unsigned long long *attn_trace() {
+    return g_trace ? g_trace + (size_t)QASA_TRACE_MAX_CTAS * QASA_TRACE_SELECT_EVENTS : nullptr;
+}
+
 // Internal status: the cooperative launch of the single-launch kernel was
 // refused (not every CTA can be resident); the caller falls back to two.
 constexpr qasa_status QASA_ERR_COOPERATIVE = static_cast<qasa_status>(100);
@@ -108,22 +116,26 @@ bool single_launch_enabled() {
     return v && v[0] == '1';
 }
 
-// Workspace carve-up: counters [units], ready flags [units] | partial (m, l)
-// [(units + C) * G * 2] | partial o [(units + C) * G * D], each region
-// 256-byte aligned.
+// Workspace carve-up: attention tickets [units] | ready flags [units] |
+// selection tickets [units] | partial (m, l) [(units + C) * G * 2] | partial o
+// [(units + C) * G * D] | score rows [units][max_pages], each region 256-byte
+// aligned.  The first three are cleared on the stream at the start of a call.
 struct WsLayout {
-    size_t counters, part_ml, part_o, total;
+    size_t counters, ready, tickets, part_ml, part_o, scores, total;
 };
 
-WsLayout ws_layout(int batch, int num_q_heads, const qasa_kv_cache *c, int grid) {
+WsLayout ws_layout(int batch, int num_q_heads, const qasa_kv_cache *c, int grid, int max_pages) {
     const size_t units = (size_t)batch * c->num_kv_heads;
     const size_t G = (size_t)(num_q_heads / c->num_kv_heads);
     const size_t slots = units + (size_t)grid;
     WsLayout w;
     w.counters = 0;
-    w.part_ml = align_up(units * 8, 256);
+    w.ready = units * 4;
+    w.tickets = units * 8;
+    w.part_ml = align_up(units * 12, 256);
     w.part_o = w.part_ml + align_up(slots * G * 2 * 4, 256);
-    w.total = w.part_o + align_up(slots * G * (size_t)c->head_dim * 4, 256);
+    w.scores = w.part_o + align_up(slots * G * (size_t)c->head_dim * 4, 256);
+    w.total = w.scores + align_up(units * (size_t)(max_pages > 0 ? max_pages : 0) * 4, 256);
     return w;
 }
 
@@ -234,8 +246,15 @@ qasa_status pool_tensor_map(CUtensorMap *map, void *base, const qasa_kv_cache *c
 qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_heads,
                        const int32_t *block_table, int max_pages, const int32_t *seq_lens,
                        const int32_t *budget_pages, int max_budget, int32_t *selected,
-                       float *scores_out, int32_t *counters, int batch, int32_t *status,
+                       float *scores_out, void *workspace, int batch, int32_t *status,
                        cudaStream_t stream) {
+    const int grid = sm_count();
+    if (grid <= 0) return QASA_ERR_CUDA;
+    const WsLayout w = ws_layout(batch, num_q_heads, cache, grid, max_pages);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    const size_t units = (size_t)batch * cache->num_kv_heads;
+    // attention tickets, ready flags and selection tickets start at zero
+    if (cudaMemsetAsync(ws, 0, units * 12, stream) != cudaSuccess) return QASA_ERR_CUDA;
     SelectParams p;
     p.bounds = cache->page_bounds;
     p.block_table = block_table;
@@ -244,8 +263,10 @@ qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_head
     p.q = q;
     p.selected = selected;
     p.scores_out = scores_out;
-    p.counters = counters;
+    p.tickets = reinterpret_cast<int32_t *>(ws + w.tickets);
+    p.scratch_scores = reinterpret_cast<float *>(ws + w.scores);
     p.status = status;
+    p.B = batch;
     p.num_phys = cache->num_phys_pages;
     p.Hkv = cache->num_kv_heads;
     p.P = cache->page_size;
@@ -254,6 +275,7 @@ qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_head
     p.max_pages = max_pages;
     p.max_budget = max_budget;
     p.scales = cache->page_scales;
+    p.trace = select_trace();
     cudaError_t e = launch_select(cache->dtype, cache->head_dim, p, batch * cache->num_kv_heads, stream);
     return e == cudaSuccess ? QASA_OK : QASA_ERR_CUDA;
 }
@@ -269,7 +291,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
                           bool fused = false, float *scores_out = nullptr) {
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    const WsLayout w = ws_layout(batch, num_q_heads, cache, grid);
+    const WsLayout w = ws_layout(batch, num_q_heads, cache, grid, max_pages);
     if (!workspace) return QASA_ERR_WORKSPACE;
     if (ws_bytes < w.total || !aligned16(workspace)) return QASA_ERR_WORKSPACE;
     CUtensorMap km, vm;
@@ -330,6 +352,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     p.scores_out = scores_out;
     p.ready = reinterpret_cast<int32_t *>(ws + w.counters) + units;
     p.scales = cache->page_scales;
+    p.trace = attn_trace();
     size_t budget = smem_optin();
     if (budget == 0) return QASA_ERR_CUDA;
     budget = budget > 1024 ? budget - 1024 : budget;   // leave room for static shared memory
@@ -419,11 +442,11 @@ qasa_status qasa_rebuild_page_bounds(const qasa_kv_cache *cache, const int32_t *
 
 size_t qasa_decode_workspace_size(int32_t batch, int32_t num_q_heads, const qasa_kv_cache *cache,
                                   int32_t max_pages_per_seq) {
-    (void)max_pages_per_seq;
     if (!cache || cache->num_kv_heads < 1 || batch < 0 || num_q_heads < cache->num_kv_heads) return 0;
+    if (max_pages_per_seq < 1 || max_pages_per_seq > kMaxPagesPerSeq) return 0;
     const int grid = sm_count();
     if (grid <= 0) return 0;
-    return ws_layout(batch, num_q_heads, cache, grid).total;
+    return ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total;
 }
 
 qasa_status qasa_select_pages(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
@@ -441,11 +464,12 @@ qasa_status qasa_select_pages(const qasa_kv_cache *cache, const void *q, int32_t
     if (!workspace) return QASA_ERR_WORKSPACE;
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    if (workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total) return QASA_ERR_WORKSPACE;
+    if (workspace_bytes < ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total ||
+        !aligned16(workspace))
+        return QASA_ERR_WORKSPACE;
     if (batch == 0) return QASA_OK;
     return run_select(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
-                      max_budget, selected, scores_out, static_cast<int32_t *>(workspace), batch,
-                      device_status, stream);
+                      max_budget, selected, scores_out, workspace, batch, device_status, stream);
 }
 
 qasa_status qasa_sparse_attention(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
@@ -464,7 +488,7 @@ qasa_status qasa_sparse_attention(const qasa_kv_cache *cache, const void *q, int
     // counters must start at zero: the selection kernel normally clears them
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total)
+    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total)
         return QASA_ERR_WORKSPACE;
     if (cudaMemsetAsync(workspace, 0, (size_t)batch * cache->num_kv_heads * 4, stream) != cudaSuccess)
         return QASA_ERR_CUDA;
@@ -489,7 +513,7 @@ qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void 
     if (max_budget < 2) return QASA_ERR_BUDGET;
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total ||
+    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total ||
         !aligned16(workspace))
         return QASA_ERR_WORKSPACE;
     if (batch == 0) return QASA_OK;
@@ -500,8 +524,7 @@ qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void 
         if (st != QASA_ERR_COOPERATIVE) return st;
     }
     st = run_select(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
-                    max_budget, selected, scores_out, static_cast<int32_t *>(workspace), batch,
-                    device_status, stream);
+                    max_budget, selected, scores_out, workspace, batch, device_status, stream);
     if (st != QASA_OK) return st;
     return run_attention(cache, q, num_q_heads, block_table, max_pages_per_seq, seq_lens, budget_pages,
                          max_budget, selected, scale, out, workspace, workspace_bytes, batch,
@@ -602,5 +625,21 @@ const char *qasa_status_string(qasa_status s) {
 }
 
 int32_t qasa_version(void) { return 100; }
+
+size_t qasa_debug_trace_bytes(void) {
+    return (size_t)QASA_TRACE_MAX_CTAS * (QASA_TRACE_SELECT_EVENTS + QASA_TRACE_ATTN_EVENTS) *
+           sizeof(unsigned long long);
+}
+
+qasa_status qasa_debug_trace(unsigned long long *buffer, size_t bytes) {
+    if (!buffer) {
+        g_trace = nullptr;
+        return QASA_OK;
+    }
+    if (reinterpret_cast<uintptr_t>(buffer) & 7u) return QASA_ERR_ALIGN;
+    if (bytes < qasa_debug_trace_bytes()) return QASA_ERR_WORKSPACE;
+    g_trace = buffer;
+    return QASA_OK;
+}
 
 }  // extern "C"

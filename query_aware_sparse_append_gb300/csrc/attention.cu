@@ -160,6 +160,12 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int C = gridDim.x, c = blockIdx.x;
     const int Hkv = p.Hkv, G = p.G;
+    unsigned long long *const tr =
+        p.trace && c < QASA_TRACE_MAX_CTAS ? p.trace + (size_t)c * QASA_TRACE_ATTN_EVENTS : nullptr;
+    if (tid == 0) {
+        trace_stamp(tr);
+        trace_smid(tr ? tr + 8 : nullptr);
+    }
 
     // warp 0 sets up the stage barriers while the other warps start the scan
     if (warp == 0) {
@@ -236,7 +242,9 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         }
     }
 
+    if (tid == 0) trace_stamp(tr ? tr + 1 : nullptr);
     pdl_wait();   // selected ids and counters come from the preceding kernel
+    if (tid == 0) trace_stamp(tr ? tr + 2 : nullptr);
 
     // locate flattened index g: sequence b, KV head h, position j in the unit
     auto locate = [&](long long g, int &b, int &h, int &j, long long &ustart, int &cnt) {
@@ -288,7 +296,9 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             sp.q = p.q;
             sp.selected = p.selected;
             sp.scores_out = p.scores_out;
-            sp.counters = p.counters;
+            sp.tickets = nullptr;
+            sp.scratch_scores = nullptr;
+            sp.B = p.B;
             sp.status = p.status;
             sp.num_phys = p.num_phys;
             sp.Hkv = Hkv;
@@ -298,6 +308,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             sp.max_pages = p.max_pages;
             sp.max_budget = p.max_budget;
             sp.scales = p.scales;
+            sp.trace = nullptr;
             BoxStage stage;
             stage.buf = sel_buf;
             stage.bar = sel_bar;
@@ -464,6 +475,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     continue;
                 }
                 if (ready) {
+                    if (tr && base == 0 && lane == 0) trace_stamp(tr + 3);
                     info[s_l].page = page;
                     info[s_l].nvalid = nvalid;
                     unsigned char *st = ring + (size_t)s_l * STAGE;
@@ -505,6 +517,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             la = lb;
             lb = lc;
         }
+        if (lane == 0) trace_stamp(tr ? tr + 5 : nullptr);
         // drain: the copies this CTA issued must land before it exits (bounded)
         __syncwarp();
         for (int s = lane; s < S; s += 32) {
@@ -655,6 +668,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     const int w = warp - 1;
     if (w == NW - 1) {
         combine_segments();
+        if (lane == 0) trace_stamp(tr ? tr + 7 : nullptr);
         return;
     }
     if (w >= NWK) return;
@@ -731,6 +745,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     *abort_flag = 1;
                     break;
                 }
+                if (tr && i == w && lane == 0) trace_stamp(tr + 4);
                 const int nvalid = info[s].nvalid;
                 unsigned char *kst = ring + (size_t)s * STAGE;
                 unsigned char *vst = kst + TILE;
@@ -999,6 +1014,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         ++kseg;
         pos = lastx;
     }
+    if (lane == 0) trace_latest(tr ? tr + 6 : nullptr);
 }
 
 // ------------------------------------------------------------------ launch

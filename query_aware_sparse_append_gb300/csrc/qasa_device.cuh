@@ -162,6 +162,22 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Diagnostics: record the current time in trace slot `t` (no-op when NULL),
+// or raise it to the current time (several writers, the latest one wins).
+__device__ __forceinline__ void trace_stamp(unsigned long long *t) {
+    if (t) *t = global_timer_ns();
+}
+__device__ __forceinline__ void trace_latest(unsigned long long *t) {
+    if (t) atomicMax(t, (unsigned long long)global_timer_ns());
+}
+__device__ __forceinline__ void trace_smid(unsigned long long *t) {
+    if (t) {
+        uint32_t id;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+        *t = id;
+    }
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");

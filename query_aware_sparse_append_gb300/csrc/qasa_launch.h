@@ -32,10 +32,12 @@ struct SelectParams {
     const void *q;
     int32_t *selected;
     float *scores_out;
-    int32_t *counters;
+    int32_t *tickets;        // [units] scored-tile counts, zero at launch (selection kernel)
+    float *scratch_scores;   // [units][max_pages] score rows when scores_out is NULL (selection kernel)
     int32_t *status;
-    int num_phys, Hkv, P, G, Hq, max_pages, max_budget;
+    int B, num_phys, Hkv, P, G, Hq, max_pages, max_budget;
     const float *scales;   // FP8 KV: [num_phys][Hkv][4] (amax K, amax V, -, -)
+    unsigned long long *trace;   // diagnostics: [QASA_TRACE_MAX_CTAS][QASA_TRACE_SELECT_EVENTS] or NULL
 };
 
 struct AttnParams {
@@ -63,6 +65,7 @@ struct AttnParams {
     float *scores_out;
     int32_t *ready;    // [units] 1 once a unit's kept ids are published (zero at launch)
     const float *scales;   // FP8 KV: [num_phys][Hkv][4] (amax K, amax V, -, -)
+    unsigned long long *trace;   // diagnostics: [QASA_TRACE_MAX_CTAS][QASA_TRACE_ATTN_EVENTS] or NULL
 };
 
 struct MassParams {

@@ -507,7 +507,8 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
 // Every thread of the group must call it with the same u.
 template <typename T, int D, bool MMA, int GMAX, class Grp>
 __device__ void select_unit(const Grp &grp, const SelectParams &p, int u, float *sc, SelScratch &x,
-                            const BoxStage *stage = nullptr, uint32_t *phase_bits = nullptr) {
+                            const BoxStage *stage = nullptr, uint32_t *phase_bits = nullptr,
+                            unsigned long long *trace_scored = nullptr) {
     const UnitPlan s = plan_unit(p, u, grp.tid == 0);
     if (s.need_scores) {
         if constexpr (MMA && !is_fp8<T>::value) {
@@ -518,6 +519,7 @@ __device__ void select_unit(const Grp &grp, const SelectParams &p, int u, float 
         }
         grp.sync();
     }
+    if (grp.tid == 0) trace_stamp(trace_scored);
     select_from_scores(grp, p, u, s, sc, x);
 }
 
@@ -635,6 +637,114 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
         }
     }
     for (int j = k + tid; j < p.max_budget; j += NT) selrow[j] = -1;
+}
+
+// ------------------------------------------------- one warp selects a unit
+
+// Selection of one unit by a single warp from its N scores in global memory
+// (written by other warps and CTAs and made visible by the caller's acquire):
+// keeps page 0, page N-1 and the (k-2) best candidates 1..N-2 (ties to the
+// lower index) and writes them ascending to selrow, -1 padded to max_budget.
+//
+// The key of the (k-2)-th best candidate (tau) is found bit by bit, from the
+// most significant bit where the smallest and the largest candidate key
+// differ: a bit is set when at least k-2 candidate keys are >= the prefix
+// with that bit set.  Keys of pages lane + 32 r, r < R, stay in registers;
+// pages beyond 32 R are re-read (L2) at every step.  An ordered ballot pass
+// then writes the kept ids: candidates above tau, the lowest-index ones equal
+// to tau up to the quota, and the two forced pages.
+template <int R>
+__device__ void warp_select_unit(const float *sc, int N, int k, int32_t *selrow, int max_budget) {
+    const int lane = threadIdx.x & 31;
+    const unsigned full = 0xffffffffu;
+    if (N <= 0) {
+        for (int j = lane; j < max_budget; j += 32) selrow[j] = -1;
+        return;
+    }
+    if (k >= N) {
+        for (int j = lane; j < max_budget; j += 32) selrow[j] = j < N ? j : -1;
+        return;
+    }
+    const int kc = k - 2;   // N >= 3 here
+    if (kc <= 0) {
+        for (int j = lane; j < max_budget; j += 32) selrow[j] = j == 0 ? 0 : (j == 1 ? N - 1 : -1);
+        return;
+    }
+    const int nslots = min(R, (N + 31) >> 5);
+    uint32_t key[R];
+    uint32_t candm = 0;   // bit r: page lane + 32 r is a candidate
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        key[r] = 0u;
+        if (r < nslots) {
+            const int j = lane + 32 * r;
+            if (j < N) key[r] = rank_key(__ldcg(sc + j));
+            if (j >= 1 && j <= N - 2) candm |= 1u << r;
+        }
+    }
+    auto cand_key = [&](int j) -> uint32_t { return rank_key(__ldcg(sc + j)); };
+    // range of the candidate keys
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if ((candm >> r) & 1u) { kmin = min(kmin, key[r]); kmax = max(kmax, key[r]); }
+    for (int j = 32 * R + lane; j <= N - 2; j += 32) {
+        const uint32_t x = cand_key(j);
+        kmin = min(kmin, x);
+        kmax = max(kmax, x);
+    }
+    kmin = __reduce_min_sync(full, kmin);
+    kmax = __reduce_max_sync(full, kmax);
+    // candidates with key >= t, over the warp
+    auto count_ge = [&](uint32_t t) -> int {
+        int cnt = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r >= nslots) break;
+            cnt += (int)(((candm >> r) & 1u) && key[r] >= t);
+        }
+        for (int j = 32 * R + lane; j <= N - 2; j += 32) cnt += (int)(cand_key(j) >= t);
+        return (int)__reduce_add_sync(full, (unsigned)cnt);
+    };
+    uint32_t tau = kmax;
+    const uint32_t diff = kmin ^ kmax;
+    if (diff) {
+        const int hb = 31 - __clz(diff);
+        uint32_t t = hb == 31 ? 0u : (kmax & ~((2u << hb) - 1u));   // common prefix, lower bits clear
+        for (int bit = hb; bit >= 0; --bit) {
+            const uint32_t t2 = t | (1u << bit);
+            if (count_ge(t2) >= kc) t = t2;
+        }
+        tau = t;
+    }
+    const int above = tau == 0xffffffffu ? 0 : count_ge(tau + 1u);
+    const int need = kc - above;   // candidates equal to tau that are kept (lowest indices)
+    // ordered compaction: page j = lane + 32 r, slot-major order is index order
+    const unsigned lt = (1u << lane) - 1u;
+    int taken = 0, eqseen = 0;
+    auto emit = [&](int j, uint32_t kj, bool cand) {
+        const bool valid = j < N;
+        const bool eq = valid && cand && kj == tau;
+        const unsigned em = __ballot_sync(full, eq);
+        const int rank = eqseen + __popc(em & lt);
+        eqseen += __popc(em);
+        const bool take = valid && (j == 0 || j == N - 1 || (cand && (kj > tau || (eq && rank < need))));
+        const unsigned tm = __ballot_sync(full, take);
+        const int pos = taken + __popc(tm & lt);
+        if (take && pos < max_budget) selrow[pos] = j;
+        taken += __popc(tm);
+    };
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (r >= nslots) break;
+        emit(lane + 32 * r, key[r], (candm >> r) & 1u);
+    }
+    for (int base = 32 * R; base < N; base += 32) {
+        const int j = base + lane;
+        const bool cand = j >= 1 && j <= N - 2;
+        emit(j, cand ? cand_key(j) : 0u, cand);
+    }
+    for (int j = k + lane; j < max_budget; j += 32) selrow[j] = -1;
 }
 
 }  // namespace qasa

@@ -97,6 +97,9 @@ def test_reference_arm_line(monkeypatch, capsys):
     assert line["value"] == 1234.5 and line["unit"] == "queries/s" and line["higher_is_better"] is True
     assert line["steps"] == 4 and line["warmup"] == 3 and line["n_gpus"] == 1
     assert line["config"]["workload"] == "headline_8k"
+    # the same config block as the GPU arm's line, key for key
+    from query_aware_sparse_append_gb300 import workloads as W
+    assert line["config"] == bench.config_block(W.CONFIGS["headline_8k"])
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == 1234.5
     assert line["e2e"] == {"value": 1234.5, "unit": "queries/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}

@@ -116,3 +116,11 @@ def test_host_call_form_query(lib, monkeypatch):
     assert f(*ptrs) == 0
     monkeypatch.setenv("QASA_HOST_DIRECT", "0")
     assert f(*ptrs) == 0
+
+
+def test_debug_trace_argument_checks(lib):
+    n = lib.debug_trace_bytes()
+    assert n == lib.TRACE_MAX_CTAS * (lib.TRACE_SELECT_EVENTS + lib.TRACE_ATTN_EVENTS) * 8
+    assert lib._lib.qasa_debug_trace(0x1004, n) == 4           # QASA_ERR_ALIGN
+    assert lib._lib.qasa_debug_trace(0x1000, n - 8) == 6       # QASA_ERR_WORKSPACE
+    assert lib._lib.qasa_debug_trace(None, 0) == 0             # off
