@@ -116,26 +116,23 @@ bool single_launch_enabled() {
     return v && v[0] == '1';
 }
 
-// Workspace carve-up: attention tickets [units] | ready flags [units] |
-// selection tickets [units] | partial (m, l) [(units + C) * G * 2] | partial o
-// [(units + C) * G * D] | score rows [units][max_pages], each region 256-byte
-// aligned.  The first three are cleared on the stream at the start of a call.
+// Workspace carve-up: counters [units], ready flags [units] | partial (m, l)
+// [(units + C) * G * 2] | partial o [(units + C) * G * D], each region
+// 256-byte aligned.
 struct WsLayout {
-    size_t counters, ready, tickets, part_ml, part_o, scores, total;
+    size_t counters, ready, part_ml, part_o, total;
 };
 
-WsLayout ws_layout(int batch, int num_q_heads, const qasa_kv_cache *c, int grid, int max_pages) {
+WsLayout ws_layout(int batch, int num_q_heads, const qasa_kv_cache *c, int grid) {
     const size_t units = (size_t)batch * c->num_kv_heads;
     const size_t G = (size_t)(num_q_heads / c->num_kv_heads);
     const size_t slots = units + (size_t)grid;
     WsLayout w;
     w.counters = 0;
     w.ready = units * 4;
-    w.tickets = units * 8;
-    w.part_ml = align_up(units * 12, 256);
+    w.part_ml = align_up(units * 8, 256);
     w.part_o = w.part_ml + align_up(slots * G * 2 * 4, 256);
-    w.scores = w.part_o + align_up(slots * G * (size_t)c->head_dim * 4, 256);
-    w.total = w.scores + align_up(units * (size_t)(max_pages > 0 ? max_pages : 0) * 4, 256);
+    w.total = w.part_o + align_up(slots * G * (size_t)c->head_dim * 4, 256);
     return w;
 }
 
@@ -248,13 +245,6 @@ qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_head
                        const int32_t *budget_pages, int max_budget, int32_t *selected,
                        float *scores_out, void *workspace, int batch, int32_t *status,
                        cudaStream_t stream) {
-    const int grid = sm_count();
-    if (grid <= 0) return QASA_ERR_CUDA;
-    const WsLayout w = ws_layout(batch, num_q_heads, cache, grid, max_pages);
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    const size_t units = (size_t)batch * cache->num_kv_heads;
-    // attention tickets, ready flags and selection tickets start at zero
-    if (cudaMemsetAsync(ws, 0, units * 12, stream) != cudaSuccess) return QASA_ERR_CUDA;
     SelectParams p;
     p.bounds = cache->page_bounds;
     p.block_table = block_table;
@@ -263,8 +253,7 @@ qasa_status run_select(const qasa_kv_cache *cache, const void *q, int num_q_head
     p.q = q;
     p.selected = selected;
     p.scores_out = scores_out;
-    p.tickets = reinterpret_cast<int32_t *>(ws + w.tickets);
-    p.scratch_scores = reinterpret_cast<float *>(ws + w.scores);
+    p.counters = static_cast<int32_t *>(workspace);   // cleared by the selection kernel
     p.status = status;
     p.B = batch;
     p.num_phys = cache->num_phys_pages;
@@ -291,7 +280,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
                           bool fused = false, float *scores_out = nullptr) {
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    const WsLayout w = ws_layout(batch, num_q_heads, cache, grid, max_pages);
+    const WsLayout w = ws_layout(batch, num_q_heads, cache, grid);
     if (!workspace) return QASA_ERR_WORKSPACE;
     if (ws_bytes < w.total || !aligned16(workspace)) return QASA_ERR_WORKSPACE;
     CUtensorMap km, vm;
@@ -350,7 +339,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     p.drain_limit_ns = kWaitLimitNs;
     p.bounds = cache->page_bounds;
     p.scores_out = scores_out;
-    p.ready = reinterpret_cast<int32_t *>(ws + w.counters) + units;
+    p.ready = reinterpret_cast<int32_t *>(ws + w.ready);
     p.scales = cache->page_scales;
     p.trace = attn_trace();
     size_t budget = smem_optin();
@@ -446,7 +435,7 @@ size_t qasa_decode_workspace_size(int32_t batch, int32_t num_q_heads, const qasa
     if (max_pages_per_seq < 1 || max_pages_per_seq > kMaxPagesPerSeq) return 0;
     const int grid = sm_count();
     if (grid <= 0) return 0;
-    return ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total;
+    return ws_layout(batch, num_q_heads, cache, grid).total;
 }
 
 qasa_status qasa_select_pages(const qasa_kv_cache *cache, const void *q, int32_t num_q_heads,
@@ -464,7 +453,7 @@ qasa_status qasa_select_pages(const qasa_kv_cache *cache, const void *q, int32_t
     if (!workspace) return QASA_ERR_WORKSPACE;
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    if (workspace_bytes < ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total ||
+    if (workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total ||
         !aligned16(workspace))
         return QASA_ERR_WORKSPACE;
     if (batch == 0) return QASA_OK;
@@ -488,7 +477,7 @@ qasa_status qasa_sparse_attention(const qasa_kv_cache *cache, const void *q, int
     // counters must start at zero: the selection kernel normally clears them
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total)
+    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total)
         return QASA_ERR_WORKSPACE;
     if (cudaMemsetAsync(workspace, 0, (size_t)batch * cache->num_kv_heads * 4, stream) != cudaSuccess)
         return QASA_ERR_CUDA;
@@ -513,7 +502,7 @@ qasa_status qasa_sparse_decode_attention(const qasa_kv_cache *cache, const void 
     if (max_budget < 2) return QASA_ERR_BUDGET;
     const int grid = sm_count();
     if (grid <= 0) return QASA_ERR_CUDA;
-    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid, max_pages_per_seq).total ||
+    if (!workspace || workspace_bytes < ws_layout(batch, num_q_heads, cache, grid).total ||
         !aligned16(workspace))
         return QASA_ERR_WORKSPACE;
     if (batch == 0) return QASA_OK;

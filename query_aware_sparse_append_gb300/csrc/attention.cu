@@ -296,8 +296,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             sp.q = p.q;
             sp.selected = p.selected;
             sp.scores_out = p.scores_out;
-            sp.tickets = nullptr;
-            sp.scratch_scores = nullptr;
+            sp.counters = p.counters;
             sp.B = p.B;
             sp.status = p.status;
             sp.num_phys = p.num_phys;
@@ -445,8 +444,12 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     row = (int)(((long long)la.phys * Hkv + la.h) * P);
                 }
             }
-            look_b(lb);
-            look_a(base + 2 * (long long)WB, lc);
+            // (the first batch is issued before the next lookups: nothing is in
+            // flight yet, so their latency would only delay the first copies)
+            if (base != 0) {
+                look_b(lb);
+                look_a(base + 2 * (long long)WB, lc);
+            }
             uint32_t s_l = stage0 + lane, ph_l = phase0;
             if (s_l >= (uint32_t)S) { s_l -= S; ph_l ^= 1u; }
             bool pending = lane < nb;
@@ -512,6 +515,10 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     pending = false;
                 }
             }
+            if (base == 0) {
+                look_b(lb);
+                look_a(2 * (long long)WB, lc);
+            }
             stage0 += nb;
             if (stage0 >= (uint32_t)S) { stage0 -= S; phase0 ^= 1u; }
             la = lb;
@@ -556,7 +563,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             const long long s1 = min(run_end(pos), ue);
             pos += s1 - g;
             const int u = b * Hkv + h;
-            if (!mbar_wait_sleepy(&seg_bar[0], kseg & 1u, p.wait_limit_ns, 256)) {
+            if (!mbar_wait_bounded(&seg_bar[0], kseg & 1u, p.wait_limit_ns)) {
                 if (lane == 0) {
                     if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
                     *abort_flag = 1;
@@ -1037,7 +1044,21 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     // bytes and need twice the stages for the same bytes in flight)
     constexpr int kMaxStages = (200 * 1024 / STAGE) < 64 ? (200 * 1024 / STAGE) : 64;
     int stages = 0, consumers = 0;
-    for (int nw = NW - 1; nw >= 1; --nw) {   // the last consumer warp is the combiner
+    // 16-bit KV: four working warps whenever the ring still holds at least four
+    // pages per warp (fewer states per unit-boundary merge; the streaming rate
+    // is the same from four warps up)
+    if constexpr (!F8) {
+        constexpr int kPreferred = 4;
+        if (kPreferred <= NW - 1) {
+            const size_t fixed = attn_smem_bytes(0, STAGE, kPreferred, GMAX, D, P, MMA, p.B, FUSED, p.max_pages,
+                                                 F8, F8CONV);
+            int s = fixed < smem_budget ? (int)((smem_budget - fixed) / per) : 0;
+            if (s > kMaxStages) s = kMaxStages;
+            s = s / kPreferred * kPreferred;
+            if (s >= 4 * kPreferred) { stages = s; consumers = kPreferred; }
+        }
+    }
+    for (int nw = NW - 1; nw >= 1 && stages == 0; --nw) {   // the last consumer warp is the combiner
         const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);

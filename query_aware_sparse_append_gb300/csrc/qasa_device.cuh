@@ -236,19 +236,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
-// Bounded wait for a warp that is off the critical path: polls with a sleep
-// between probes so that it does not take issue slots from the warps that are.
-__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
-                                                 unsigned sleep_ns) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        __nanosleep(sleep_ns);
-        if (mbar_test_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > limit_ns) return false;
-    }
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

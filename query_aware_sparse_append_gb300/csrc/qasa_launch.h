@@ -32,8 +32,7 @@ struct SelectParams {
     const void *q;
     int32_t *selected;
     float *scores_out;
-    int32_t *tickets;        // [units] scored-tile counts, zero at launch (selection kernel)
-    float *scratch_scores;   // [units][max_pages] score rows when scores_out is NULL (selection kernel)
+    int32_t *counters;       // [units] the attention kernel's page tickets, cleared here
     int32_t *status;
     int B, num_phys, Hkv, P, G, Hq, max_pages, max_budget;
     const float *scales;   // FP8 KV: [num_phys][Hkv][4] (amax K, amax V, -, -)

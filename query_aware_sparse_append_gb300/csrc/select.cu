@@ -11,177 +11,174 @@
 // page N-1, and the best (k - 2) remaining pages (ties to the lower index),
 // written as ascending logical ids.
 //
-// Work split (persistent, balanced over pages).  The 16-page tiles of every
-// (sequence, KV head) unit that needs scores are laid out in one flattened
-// order (unit-major); warp w of the grid's W warps scores the contiguous tile
-// range [w*T/W, (w+1)*T/W) into the unit's score row in global memory (L2),
-// then adds the number of tiles it scored to the unit's ticket
-// (acquire-release).  The warp that completes a unit's ticket selects that
-// unit on its own (warp_select_unit) while the other warps keep streaming
-// page boxes, so the selection does not leave HBM idle and ragged batches
-// spread evenly over the SMs.  Units that need no scores (no pages, or every
-// page kept) are written directly.  The scoring paths (tensor-core
-// contraction through the sign split, or FFMA) live in select_device.cuh,
-// shared with the single-launch decode kernel.
+// One CTA per (sequence, KV head), or a cluster of C CTAs per (sequence, KV
+// head) that split its 16-page tiles evenly and store their scores straight
+// into the first CTA's shared memory (distributed shared memory), which then
+// selects; the scoring paths (tensor-core contraction through the sign split,
+// or FFMA) and the radix selection live in select_device.cuh, shared with the
+// single-launch decode kernel.
 #include <cstdlib>
 
 #include "select_device.cuh"
 
 namespace qasa {
 
-constexpr int kSelWarps = 8;          // warps per CTA
-constexpr int kSelCtasPerSm = 2;      // resident CTAs per SM (16 warps: one box tile in flight each)
-constexpr int kSelKeySlots = 32;      // keys per lane the selecting warp keeps in registers (N <= 1024)
 
-// One warp scoring on its own (the scoring paths stride tiles by the group's
-// warp count; here that count is one).
-struct OneWarp {
-    int tid;   // lane
-    __device__ __forceinline__ void sync() const { __syncwarp(); }
-    __device__ __forceinline__ int lane() const { return tid; }
-    __device__ __forceinline__ int warp() const { return 0; }
-    static constexpr int warps = 1;
-};
-
-template <typename T, int D, bool MMA, int GMAX>
-__global__ void __launch_bounds__(32 * kSelWarps, kSelCtasPerSm) select_tiles_kernel(SelectParams p) {
-    extern __shared__ __align__(16) int sm_i[];
-    int *prefix = sm_i;                 // [B + 1] scored tiles of the sequences before b (one KV head)
-    int *npages = prefix + p.B + 1;     // [B] pages of sequence b
-    __shared__ int s_wsum[kSelWarps];
+// NT threads per (sequence, KV head): 128, 256 or 512 (see launch_select_t).
+template <typename T, int D, bool MMA, int GMAX, int NT>
+__global__ void __launch_bounds__(NT, NT >= 512 ? 1 : 512 / NT) select_kernel(SelectParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float *sc = reinterpret_cast<float *>(smem_raw);   // [max_pages] scores, then keys in place
+    __shared__ SelScratch scratch;
 
     pdl_launch_dependents();
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int C = gridDim.x, c = blockIdx.x;
-    const int Hkv = p.Hkv, B = p.B;
-    unsigned long long *const tr =
-        p.trace && c < QASA_TRACE_MAX_CTAS ? p.trace + (size_t)c * QASA_TRACE_SELECT_EVENTS : nullptr;
-    if (tid == 0) {
+    const int u = blockIdx.x;
+    unsigned long long *tr =
+        p.trace && blockIdx.x < QASA_TRACE_MAX_CTAS ? p.trace + (size_t)blockIdx.x * QASA_TRACE_SELECT_EVENTS : nullptr;
+    if (threadIdx.x == 0) {
+        trace_stamp(tr);
+        trace_smid(tr ? tr + 3 : nullptr);
+        p.counters[u] = 0;
+    }
+    const SelGroup<NT, -1> grp{(int)threadIdx.x};
+    select_unit<T, D, MMA, GMAX>(grp, p, u, sc, scratch, nullptr, nullptr, tr ? tr + 1 : nullptr);
+    if (tr) {
+        __syncthreads();
+        if (threadIdx.x == 0) trace_stamp(tr + 2);
+    }
+}
+
+// CTAs per unit of the cluster form
+constexpr int kSplit = 4;
+
+// ---- thread-block cluster primitives (PTX ISA: barrier.cluster, mapa)
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Generic address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ float *cluster_map(float *local, uint32_t rank) {
+    uint64_t out;
+    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+    return reinterpret_cast<float *>(out);
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// C CTAs of NT threads per (sequence, KV head), launched as clusters of C:
+// CTA r scores tiles [r*T/C, (r+1)*T/C) of the unit's T tiles into CTA 0's
+// score array; after the cluster barrier CTA 0 selects.  Every thread of every
+// CTA passes both cluster barriers (the arrive at entry / wait before the first
+// remote store makes sure each CTA of the cluster is running; the second makes
+// the scores visible to CTA 0), so no CTA exits while another still writes
+// into its shared memory.
+template <typename T, int D, bool MMA, int GMAX, int NT, int C>
+__global__ void __launch_bounds__(NT, NT >= 512 ? 1 : 512 / NT) select_cluster_kernel(SelectParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float *sc = reinterpret_cast<float *>(smem_raw);   // [max_pages], used by CTA 0
+    __shared__ SelScratch scratch;
+
+    cluster_arrive_relaxed();
+    pdl_launch_dependents();
+
+    const int u = blockIdx.x / C;
+    const uint32_t rank = cluster_ctarank();
+    unsigned long long *tr =
+        p.trace && blockIdx.x < QASA_TRACE_MAX_CTAS ? p.trace + (size_t)blockIdx.x * QASA_TRACE_SELECT_EVENTS : nullptr;
+    if (threadIdx.x == 0) {
         trace_stamp(tr);
         trace_smid(tr ? tr + 3 : nullptr);
     }
-
-    // page counts and the scored-tile prefix over the sequences (every CTA;
-    // CTA 0 reports length and budget errors, once per sequence)
-    {
-        int carry = 0;
-        for (int base = 0; base < B; base += blockDim.x) {
-            const int b = base + tid;
-            int cnt = 0;
-            if (b < B) {
-                const int L = valid_len(p.seq_lens[b], p.max_pages, p.P, c == 0 ? p.status : nullptr);
-                const int N = (L + p.P - 1) / p.P;
-                const int k = kept_pages(N, p.budget[b], p.max_budget, p.status, c == 0);
-                npages[b] = N;
-                cnt = (N > 0 && (k < N || p.scores_out != nullptr)) ? (N + 15) >> 4 : 0;
-            }
-            int incl = cnt;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int x = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += x;
-            }
-            if (lane == 31) s_wsum[warp] = incl;
-            __syncthreads();
-            int wbase = 0, total = 0;
-#pragma unroll
-            for (int w = 0; w < kSelWarps; ++w) {
-                const int v = s_wsum[w];
-                wbase += w < warp ? v : 0;
-                total += v;
-            }
-            if (b < B) prefix[b] = carry + wbase + incl - cnt;
-            carry += total;
-            __syncthreads();
-        }
-        if (tid == 0) prefix[B] = carry;
+    if (rank == 0 && threadIdx.x == 0) p.counters[u] = 0;
+    const SelGroup<NT, -1> grp{(int)threadIdx.x};
+    const UnitPlan s = plan_unit(p, u, rank == 0 && threadIdx.x == 0);
+    float *lead = cluster_map(sc, 0);
+    cluster_wait_acquire();
+    if (s.need_scores) {
+        const int tiles = (s.N + 15) >> 4;
+        score_window<T, D, MMA, GMAX>(grp, p, s, lead, (int)rank * tiles / C, ((int)rank + 1) * tiles / C);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (threadIdx.x == 0) trace_stamp(tr ? tr + 1 : nullptr);
+    if (rank != 0) return;
+    select_from_scores(grp, p, u, s, sc, scratch);
+    if (tr) {
         __syncthreads();
+        if (threadIdx.x == 0) trace_stamp(tr + 2);
     }
-
-    // units whose kept set needs no scores: no pages (all -1) or every page kept
-    const int units = B * Hkv;
-    for (int u = c; u < units; u += C) {
-        const int b = u / Hkv;
-        if (prefix[b + 1] != prefix[b]) continue;
-        const int N = npages[b];
-        int32_t *row = p.selected + (size_t)u * p.max_budget;
-        for (int j = tid; j < p.max_budget; j += blockDim.x) row[j] = j < N ? j : -1;
-    }
-
-    // this warp's range of the flattened tiles
-    const long long Tt = (long long)Hkv * prefix[B];
-    const int GW = C * kSelWarps, gw = c * kSelWarps + warp;
-    long long t = (long long)gw * Tt / GW;
-    const long long t1 = (long long)(gw + 1) * Tt / GW;
-    const OneWarp one{lane};
-    float *const score_base = p.scores_out ? p.scores_out : p.scratch_scores;
-    while (t < t1) {
-        int lo = 0, hi = B - 1;   // largest b with Hkv * prefix[b] <= t
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((long long)Hkv * prefix[mid] <= t) lo = mid; else hi = mid - 1;
-        }
-        const int b = lo;
-        const int cnt = prefix[b + 1] - prefix[b];          // tiles per unit of sequence b (> 0 here)
-        const long long off = t - (long long)Hkv * prefix[b];
-        const int h = (int)(off / cnt);
-        const int j0 = (int)(off - (long long)h * cnt);
-        const long long ue = (long long)Hkv * prefix[b] + (long long)(h + 1) * cnt;
-        const long long s1 = ue < t1 ? ue : t1;
-        const int j1 = j0 + (int)(s1 - t);
-        const int u = b * Hkv + h;
-        UnitPlan s;
-        s.b = b;
-        s.h = h;
-        s.N = npages[b];
-        s.k = 0;
-        s.need_scores = true;
-        float *sc = score_base + (size_t)u * p.max_pages;
-        score_window<T, D, MMA, GMAX>(one, p, s, sc, j0, j1);
-        if (s1 == t1 && lane == 0) trace_latest(tr ? tr + 1 : nullptr);
-        // publish this warp's scores and count its tiles; the warp that
-        // completes the unit selects it
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            const int n = j1 - j0;
-            last = atomic_add_acq_rel_gpu(&p.tickets[u], n) + n == cnt;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __syncwarp();
-            const int k = kept_pages(s.N, p.budget[b], p.max_budget, nullptr, false);
-            warp_select_unit<kSelKeySlots>(sc, s.N, k, p.selected + (size_t)u * p.max_budget, p.max_budget);
-        }
-        t = s1;
-    }
-    if (lane == 0) trace_latest(tr ? tr + 2 : nullptr);
 }
 
-template <typename T, int D, bool MMA, int GMAX>
-static cudaError_t launch_select_t(const SelectParams &p, int units, cudaStream_t stream) {
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-        sms = 1;
-    // one warp per tile at most: small batches launch fewer CTAs
-    const long long max_tiles = (long long)units * ((p.max_pages + 15) / 16);
-    long long grid = (max_tiles + kSelWarps - 1) / kSelWarps;
-    if (grid > (long long)kSelCtasPerSm * sms) grid = (long long)kSelCtasPerSm * sms;
-    if (const char *f = std::getenv("QASA_SELECT_CTAS")) {   // diagnostic: force the grid size
-        const long long want = std::atoll(f);
-        if (want >= 1 && want <= 65535) grid = want;
+template <typename T, int D, bool MMA, int GMAX, int NT>
+static cudaError_t launch_select_nt(const SelectParams &p, int units, int split, cudaStream_t stream) {
+    const size_t smem = (size_t)p.max_pages * sizeof(float);
+    if (split == 1) {
+        auto kern = select_kernel<T, D, MMA, GMAX, NT>;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        kern<<<units, NT, smem, stream>>>(p);
+        return cudaGetLastError();
     }
-    if (grid < 1) grid = 1;
-    const size_t smem = (size_t)(2 * p.B + 1) * sizeof(int);
-    auto kern = select_tiles_kernel<T, D, MMA, GMAX>;
+    void (*kern)(SelectParams) = select_cluster_kernel<T, D, MMA, GMAX, NT, kSplit>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    kern<<<(unsigned)grid, 32 * kSelWarps, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * split));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <typename T, int D, bool MMA, int GMAX>
+static cudaError_t launch_select_t(const SelectParams &p, int units, cudaStream_t stream) {
+    // Few units for the SMs: give each more warps (its scoring is a per-warp
+    // chain of dependent tile loads); many units: 4 warps each keeps several
+    // units resident per SM, which hides that latency better.
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        sms = 1;
+    // Few units (a small batch): kSplit CTAs per unit, as a cluster, so the
+    // scoring of one unit runs on several SMs.  With units for every SM the
+    // split only adds launch and cluster-scheduling cost.
+    int split = units * kSplit <= sms ? kSplit : 1;
+    if (const char *f = std::getenv("QASA_SELECT_SPLIT")) {     // diagnostic: force CTAs per unit
+        const int want = std::atoi(f);
+        if (want == 1 || want == kSplit) split = want;
+    }
+    const int ctas = units * split;
+    int nt = ctas * 2 <= sms ? 512 : ctas <= 2 * sms ? 256 : 128;
+    if (const char *f = std::getenv("QASA_SELECT_THREADS")) {   // diagnostic: force the CTA size
+        const int want = std::atoi(f);
+        if (want == 128 || want == 256 || want == 512) nt = want;
+    }
+    if (nt == 512) return launch_select_nt<T, D, MMA, GMAX, 512>(p, units, split, stream);
+    if (nt == 256) return launch_select_nt<T, D, MMA, GMAX, 256>(p, units, split, stream);
+    return launch_select_nt<T, D, MMA, GMAX, 128>(p, units, split, stream);
 }
 
 cudaError_t launch_select(qasa_dtype dt, int D, const SelectParams &p, int units,

@@ -56,10 +56,17 @@ struct SelGroup {
 };
 
 // Shared scratch of one group: histogram, per-warp totals, search results.
+constexpr int kSelBins = 1024;   // histogram bins of the selection (10-bit digits)
+
 struct SelScratch {
-    int hist[256];
+    union {
+        int hist[kSelBins];
+        uint32_t list[kSelBins];   // keys sharing the final prefix (once the histogram is done)
+    };
     int warp_tot[32];
-    int digit, above;
+    uint32_t kmin[32], kmax[32];
+    int digit, above, cnt;
+    uint32_t tau;
 };
 
 // Key whose unsigned order is the ranking order: larger score first; -0 and +0
@@ -524,12 +531,24 @@ __device__ void select_unit(const Grp &grp, const SelectParams &p, int u, float 
 }
 
 // The unit's selection once sc[0, N) holds its scores (when s.need_scores).
+//
+// tau, the key of the (k-2)-th best candidate, is narrowed down digit by
+// digit over the bits where the candidate keys differ: a 1024-bin shared
+// histogram of the next 10 bits of the keys sharing the prefix found so far
+// gives the digit that holds the wanted rank.  Once no more keys share the
+// prefix than the group has threads, they are gathered, one per thread, and
+// the key of the wanted rank is read off by comparing every pair.  Ordered
+// scans over contiguous index segments then keep every candidate above tau,
+// the lowest-index ones equal to it, and the two forced pages, in ascending
+// order.
 template <class Grp>
 __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u, const UnitPlan &s, float *sc,
                                    SelScratch &x) {
     uint32_t *keys = reinterpret_cast<uint32_t *>(sc);
     constexpr int NT = Grp::warps * 32;
-    const int tid = grp.tid, lane = grp.lane();
+    constexpr int BPT = kSelBins / NT;   // histogram bins per thread (NT <= 1024)
+    static_assert(kSelBins % NT == 0, "bins split evenly over the group");
+    const int tid = grp.tid, lane = grp.lane(), warp = grp.warp();
     const int N = s.N, k = s.k;
     int32_t *selrow = p.selected + (size_t)u * p.max_budget;
 
@@ -543,71 +562,115 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
         for (int j = tid; j < p.max_budget; j += NT) selrow[j] = j < N ? j : -1;
         return;
     }
-    // here N >= 2: forced pages {0, N-1}; candidates 1..N-2; choose kc of them
+    // here N >= 3: forced pages {0, N-1}; candidates 1..N-2; choose kc of them
     const int kc = k - 2;
     const int last = N - 1;
     if (kc == 0) {
         for (int j = tid; j < p.max_budget; j += NT) selrow[j] = j == 0 ? 0 : (j == 1 ? last : -1);
         return;
     }
-    for (int i = tid; i < N; i += NT) keys[i] = rank_key(sc[i]);
-    grp.sync();
-
-    // radix select: tau = key of the kc-th largest candidate
-    uint32_t prefix = 0, pmask = 0;
-    int need = kc;
-    const int iters = (N - 2 + NT - 1) / NT;
-#pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += NT) x.hist[i] = 0;
-        grp.sync();
-        for (int it = 0; it < iters; ++it) {
-            const int i = 1 + it * NT + tid;
-            const bool in = i <= N - 2;
-            const uint32_t key = in ? keys[i] : 0u;
-            const bool match = in && ((key & pmask) == prefix);
-            const unsigned active = __ballot_sync(0xffffffffu, match);
-            if (match) {
-                const int digit = (key >> shift) & 255;
-                const unsigned peers = __match_any_sync(active, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&x.hist[digit], __popc(peers));
-            }
-        }
-        grp.sync();
-        if (grp.warp() == 0) {
-            int cnt[8], tot = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) { cnt[j] = x.hist[255 - 8 * lane - j]; tot += cnt[j]; }
-            int incl = tot;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                int t = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += t;
-            }
-            const int excl = incl - tot;
-            if (excl < need && need <= incl) {
-                int run = excl;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (run + cnt[j] >= need) { x.digit = 255 - 8 * lane - j; x.above = run; break; }
-                    run += cnt[j];
-                }
-            }
-        }
-        grp.sync();
-        need -= x.above;
-        prefix |= (uint32_t)x.digit << shift;
-        pmask |= 0xffu << shift;
-    }
-    const uint32_t tau = prefix;   // `need` candidates equal to tau are kept (lowest indices)
-
-    // ordered passes over contiguous index segments: rank among equals, then compaction
+    // contiguous index segment of this thread; keys in place of the scores
     const int E = (N + NT - 1) / NT;
     const int i0 = min(N, tid * E), i1 = min(N, i0 + E);
-    int eq = 0;
-    for (int i = i0; i < i1; ++i)
-        if (i >= 1 && i <= N - 2 && keys[i] == tau) ++eq;
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t key = rank_key(sc[i]);
+        keys[i] = key;
+        if (i >= 1 && i <= N - 2) { lo = min(lo, key); hi = max(hi, key); }
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) { x.kmin[warp] = lo; x.kmax[warp] = hi; }
+    grp.sync();
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int w = 0; w < Grp::warps; ++w) { kmin = min(kmin, x.kmin[w]); kmax = max(kmax, x.kmax[w]); }
+
+    uint32_t tau = kmax;
+    if (kmin != kmax) {
+        const int hb = 31 - __clz(kmin ^ kmax);
+        uint32_t pmask = hb == 31 ? 0u : ~((2u << hb) - 1u);   // bits shared by every candidate
+        uint32_t prefix = kmax & pmask;
+        int need = kc;     // rank (1 = largest) of tau among the keys matching (prefix, pmask)
+        int low = hb + 1;  // bits [low, 32) of tau are known
+        int m = 0;         // keys matching the prefix
+        while (true) {
+            const int shift = low > 10 ? low - 10 : 0;
+            const uint32_t dmask = (1u << (low - shift)) - 1u;
+            for (int i = tid; i < kSelBins; i += NT) x.hist[i] = 0;
+            grp.sync();
+            for (int i = max(i0, 1); i < min(i1, N - 1); ++i) {
+                const uint32_t key = keys[i];
+                if ((key & pmask) == prefix) atomicAdd(&x.hist[(key >> shift) & dmask], 1);
+            }
+            grp.sync();
+            // thread t holds bins kSelBins-1-BPT*t .. kSelBins-BPT*(t+1) (descending digits)
+            int c[BPT], tot = 0;
+#pragma unroll
+            for (int j = 0; j < BPT; ++j) {
+                c[j] = x.hist[kSelBins - 1 - BPT * tid - j];
+                tot += c[j];
+            }
+            const int excl = group_excl_scan(grp, tot, x.warp_tot);
+            if (excl < need && need <= excl + tot) {
+                int run = excl;
+#pragma unroll
+                for (int j = 0; j < BPT; ++j) {
+                    if (run + c[j] >= need) {
+                        x.digit = kSelBins - 1 - BPT * tid - j;
+                        x.above = run;
+                        x.cnt = c[j];
+                        break;
+                    }
+                    run += c[j];
+                }
+            }
+            grp.sync();
+            const int dig = x.digit;
+            need -= x.above;
+            m = x.cnt;
+            prefix |= (uint32_t)dig << shift;
+            pmask |= dmask << shift;
+            low = shift;
+            grp.sync();   // the scratch is reused below
+            if (low == 0 || m <= NT) break;
+        }
+        if (low == 0) {
+            tau = prefix;
+        } else {
+            // gather the m <= NT keys sharing the prefix and read off rank `need`
+            int mine = 0;
+            for (int i = max(i0, 1); i < min(i1, N - 1); ++i) mine += (int)((keys[i] & pmask) == prefix);
+            int at = group_excl_scan(grp, mine, x.warp_tot);
+            for (int i = max(i0, 1); i < min(i1, N - 1); ++i)
+                if ((keys[i] & pmask) == prefix) x.list[at++] = keys[i];
+            grp.sync();
+            if (tid < m) {
+                const uint32_t v = x.list[tid];
+                int gt = 0, eq = 0;
+                for (int j = 0; j < m; ++j) {
+                    const uint32_t w = x.list[j];
+                    gt += w > v;
+                    eq += w == v;
+                }
+                if (gt < need && need <= gt + eq) x.tau = v;   // every writer writes the same value
+            }
+            grp.sync();
+            tau = x.tau;
+        }
+    }
+
+    // candidates above tau are kept; of those equal to tau, the lowest indices
+    // up to the quota: need_eq = kc - (candidates above tau)
+    int gt = 0, eq = 0;
+    for (int i = max(i0, 1); i < min(i1, N - 1); ++i) {
+        gt += (int)(keys[i] > tau);
+        eq += (int)(keys[i] == tau);
+    }
+    const int above_before = group_excl_scan(grp, gt, x.warp_tot);
+    const int n_above = above_before + gt;   // valid in the last thread only: broadcast below
+    if (tid == NT - 1) x.above = n_above;
     int eq_rank = group_excl_scan(grp, eq, x.warp_tot);
+    const int need_eq = kc - x.above;
     int kept = 0;
     {
         int r = eq_rank;
@@ -616,7 +679,7 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
             if (i == 0 || i == last) take = true;
             else {
                 const uint32_t key = keys[i];
-                take = key > tau || (key == tau && r < need);
+                take = key > tau || (key == tau && r < need_eq);
                 if (key == tau) ++r;
             }
             kept += take;
@@ -630,121 +693,13 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
             if (i == 0 || i == last) take = true;
             else {
                 const uint32_t key = keys[i];
-                take = key > tau || (key == tau && r < need);
+                take = key > tau || (key == tau && r < need_eq);
                 if (key == tau) ++r;
             }
             if (take && pos < p.max_budget) selrow[pos++] = i;
         }
     }
     for (int j = k + tid; j < p.max_budget; j += NT) selrow[j] = -1;
-}
-
-// ------------------------------------------------- one warp selects a unit
-
-// Selection of one unit by a single warp from its N scores in global memory
-// (written by other warps and CTAs and made visible by the caller's acquire):
-// keeps page 0, page N-1 and the (k-2) best candidates 1..N-2 (ties to the
-// lower index) and writes them ascending to selrow, -1 padded to max_budget.
-//
-// The key of the (k-2)-th best candidate (tau) is found bit by bit, from the
-// most significant bit where the smallest and the largest candidate key
-// differ: a bit is set when at least k-2 candidate keys are >= the prefix
-// with that bit set.  Keys of pages lane + 32 r, r < R, stay in registers;
-// pages beyond 32 R are re-read (L2) at every step.  An ordered ballot pass
-// then writes the kept ids: candidates above tau, the lowest-index ones equal
-// to tau up to the quota, and the two forced pages.
-template <int R>
-__device__ void warp_select_unit(const float *sc, int N, int k, int32_t *selrow, int max_budget) {
-    const int lane = threadIdx.x & 31;
-    const unsigned full = 0xffffffffu;
-    if (N <= 0) {
-        for (int j = lane; j < max_budget; j += 32) selrow[j] = -1;
-        return;
-    }
-    if (k >= N) {
-        for (int j = lane; j < max_budget; j += 32) selrow[j] = j < N ? j : -1;
-        return;
-    }
-    const int kc = k - 2;   // N >= 3 here
-    if (kc <= 0) {
-        for (int j = lane; j < max_budget; j += 32) selrow[j] = j == 0 ? 0 : (j == 1 ? N - 1 : -1);
-        return;
-    }
-    const int nslots = min(R, (N + 31) >> 5);
-    uint32_t key[R];
-    uint32_t candm = 0;   // bit r: page lane + 32 r is a candidate
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        key[r] = 0u;
-        if (r < nslots) {
-            const int j = lane + 32 * r;
-            if (j < N) key[r] = rank_key(__ldcg(sc + j));
-            if (j >= 1 && j <= N - 2) candm |= 1u << r;
-        }
-    }
-    auto cand_key = [&](int j) -> uint32_t { return rank_key(__ldcg(sc + j)); };
-    // range of the candidate keys
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        if ((candm >> r) & 1u) { kmin = min(kmin, key[r]); kmax = max(kmax, key[r]); }
-    for (int j = 32 * R + lane; j <= N - 2; j += 32) {
-        const uint32_t x = cand_key(j);
-        kmin = min(kmin, x);
-        kmax = max(kmax, x);
-    }
-    kmin = __reduce_min_sync(full, kmin);
-    kmax = __reduce_max_sync(full, kmax);
-    // candidates with key >= t, over the warp
-    auto count_ge = [&](uint32_t t) -> int {
-        int cnt = 0;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (r >= nslots) break;
-            cnt += (int)(((candm >> r) & 1u) && key[r] >= t);
-        }
-        for (int j = 32 * R + lane; j <= N - 2; j += 32) cnt += (int)(cand_key(j) >= t);
-        return (int)__reduce_add_sync(full, (unsigned)cnt);
-    };
-    uint32_t tau = kmax;
-    const uint32_t diff = kmin ^ kmax;
-    if (diff) {
-        const int hb = 31 - __clz(diff);
-        uint32_t t = hb == 31 ? 0u : (kmax & ~((2u << hb) - 1u));   // common prefix, lower bits clear
-        for (int bit = hb; bit >= 0; --bit) {
-            const uint32_t t2 = t | (1u << bit);
-            if (count_ge(t2) >= kc) t = t2;
-        }
-        tau = t;
-    }
-    const int above = tau == 0xffffffffu ? 0 : count_ge(tau + 1u);
-    const int need = kc - above;   // candidates equal to tau that are kept (lowest indices)
-    // ordered compaction: page j = lane + 32 r, slot-major order is index order
-    const unsigned lt = (1u << lane) - 1u;
-    int taken = 0, eqseen = 0;
-    auto emit = [&](int j, uint32_t kj, bool cand) {
-        const bool valid = j < N;
-        const bool eq = valid && cand && kj == tau;
-        const unsigned em = __ballot_sync(full, eq);
-        const int rank = eqseen + __popc(em & lt);
-        eqseen += __popc(em);
-        const bool take = valid && (j == 0 || j == N - 1 || (cand && (kj > tau || (eq && rank < need))));
-        const unsigned tm = __ballot_sync(full, take);
-        const int pos = taken + __popc(tm & lt);
-        if (take && pos < max_budget) selrow[pos] = j;
-        taken += __popc(tm);
-    };
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        if (r >= nslots) break;
-        emit(lane + 32 * r, key[r], (candm >> r) & 1u);
-    }
-    for (int base = 32 * R; base < N; base += 32) {
-        const int j = base + lane;
-        const bool cand = j >= 1 && j <= N - 2;
-        emit(j, cand ? cand_key(j) : 0u, cand);
-    }
-    for (int j = k + lane; j < max_budget; j += 32) selrow[j] = -1;
 }
 
 }  // namespace qasa

@@ -1,13 +1,13 @@
-"""Page selection is independent of how its work is split over the grid.
+"""Page selection by one CTA per unit against a cluster of CTAs per unit.
 
-The selection kernel splits the flattened 16-page tiles of all units over the
-warps of its grid; a unit's tiles may be scored by several warps of several
-CTAs, and the warp whose tile count completes the unit's ticket selects it.
-QASA_SELECT_CTAS forces the grid size, which moves every split point and
-every ticket winner.  Every page score is computed by the same code whichever
-warp runs its tile, so scores and kept ids must agree bit for bit across grid
-sizes, and the decode step's output too (the attention kernel is the same).
-The other GPU tests check the selection against the oracle.
+For small batches qasa_select_pages runs every (sequence, KV head) on a
+cluster of four CTAs that score a quarter of its 16-page tiles each into the
+first CTA's shared memory, which then selects; for large batches one CTA
+scores and selects a unit.  QASA_SELECT_SPLIT forces either form.  Every page
+score is computed by the same code whichever CTA runs it, so scores and kept
+ids must agree bit for bit, and the decode step's output too (the attention
+kernel is the same).  The other GPU tests check both forms against the oracle:
+their small batches take the cluster form, the bench-sized ones the other.
 """
 import dataclasses
 
@@ -28,12 +28,9 @@ def _lib():
     build.build()
 
 
-def _select(case, ctas, monkeypatch):
+def _select(case, split, monkeypatch):
     from query_aware_sparse_append_gb300 import binding as qasa
-    if ctas:
-        monkeypatch.setenv("QASA_SELECT_CTAS", str(ctas))
-    else:
-        monkeypatch.delenv("QASA_SELECT_CTAS", raising=False)
+    monkeypatch.setenv("QASA_SELECT_SPLIT", str(split))
     maxp = case.bt.shape[1]
     sc = torch.full((case.cfg.batch, case.cfg.num_kv_heads, maxp), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -59,14 +56,13 @@ def _bits(t):
     ("gpt2_345m", None, 2, None, None),                      # G = 1, 16 KV heads
     ("serving_mix", None, 7, [0, 700, 16384, 17, 513, 9000, 33], [5, 1000, 100, 3, 2, 1, 40]),
 ])
-def test_selection_does_not_depend_on_the_grid(name, dtype, batch, lens, budgets, monkeypatch):
+def test_cluster_selection_equals_one_cta_per_unit(name, dtype, batch, lens, budgets, monkeypatch):
     cfg = W.CONFIGS[name]
     if dtype:
         cfg = dataclasses.replace(cfg, dtype=dtype)
     case = H.make_case(cfg, seed=81, batch=batch, lens=lens, budgets=budgets)
-    s0, c0, o0 = _select(case, None, monkeypatch)
-    for ctas in (1, 3, 37, 304):
-        s1, c1, o1 = _select(case, ctas, monkeypatch)
-        assert torch.equal(s0, s1), "kept ids differ with %d CTAs" % ctas
-        assert torch.equal(_bits(c0), _bits(c1)), "scores differ with %d CTAs" % ctas
-        assert torch.equal(_bits(o0), _bits(o1))
+    s1, c1, o1 = _select(case, 1, monkeypatch)
+    s4, c4, o4 = _select(case, 4, monkeypatch)
+    assert torch.equal(s1, s4), "kept ids differ between the two forms"
+    assert torch.equal(_bits(c1), _bits(c4)), "scores differ between the two forms"
+    assert torch.equal(_bits(o1), _bits(o4))
