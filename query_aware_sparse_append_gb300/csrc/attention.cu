@@ -70,7 +70,7 @@ size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int
     s += (size_t)(2 * B + 2) * sizeof(int);            // prefix, lengths
     if (fused) {
         // selector scratch: scores, block-table row, box staging slots + barriers
-        s += 16 + (size_t)max_pages * sizeof(float) + sizeof(SelScratch);
+        s += 16 + (size_t)max_pages * sizeof(float) + 16 + sizeof(SelScratch);
         s += 16 + (size_t)max_pages * sizeof(int32_t);
         if (mma) s += 16 + (size_t)kSelStageSlots * (16 * (2 * D * 2 + 64) + sizeof(uint64_t));
     }
@@ -139,7 +139,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     // unit's block-table row [max_pages] and (tensor-core scoring) the box
     // staging slots with their barriers
     float *sel_sc = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(lens + p.B) + 15) & ~uintptr_t(15));
-    SelScratch *sel_x = reinterpret_cast<SelScratch *>(sel_sc + (FUSED ? p.max_pages : 0));
+    SelScratch *sel_x = reinterpret_cast<SelScratch *>(
+        (reinterpret_cast<uintptr_t>(sel_sc + (FUSED ? p.max_pages : 0)) + 15) & ~uintptr_t(15));
     int32_t *sel_phys = reinterpret_cast<int32_t *>(
         (reinterpret_cast<uintptr_t>(sel_x + (FUSED ? 1 : 0)) + 15) & ~uintptr_t(15));
     unsigned char *sel_buf = reinterpret_cast<unsigned char *>(

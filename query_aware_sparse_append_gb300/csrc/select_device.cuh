@@ -58,14 +58,14 @@ struct SelGroup {
 // Shared scratch of one group: histogram, per-warp totals, search results.
 constexpr int kSelBins = 1024;   // histogram bins of the selection (10-bit digits)
 
-struct SelScratch {
+struct __align__(16) SelScratch {
     union {
         int hist[kSelBins];
         uint32_t list[kSelBins];   // keys sharing the final prefix (once the histogram is done)
     };
     int warp_tot[32];
     uint32_t kmin[32], kmax[32];
-    int digit, above, cnt;
+    int digit, above, cnt, gathered;
     uint32_t tau;
 };
 
@@ -93,6 +93,29 @@ __device__ __forceinline__ int group_excl_scan(const Grp &g, int v, int *warp_to
     int base = 0;
     for (int w = 0; w < warp; ++w) base += warp_tot[w];
     g.sync();
+    return base + incl - v;
+}
+
+// Exclusive scan over the threads of the group, and the group's total.
+template <class Grp>
+__device__ __forceinline__ int group_excl_scan_total(const Grp &g, int v, int *warp_tot, int &total) {
+    const int lane = g.lane(), warp = g.warp();
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    g.sync();
+    int base = 0, tot = 0;
+    for (int w = 0; w < Grp::warps; ++w) {
+        const int x = warp_tot[w];
+        base += w < warp ? x : 0;
+        tot += x;
+    }
+    g.sync();
+    total = tot;
     return base + incl - v;
 }
 
@@ -535,19 +558,21 @@ __device__ void select_unit(const Grp &grp, const SelectParams &p, int u, float 
 // tau, the key of the (k-2)-th best candidate, is narrowed down digit by
 // digit over the bits where the candidate keys differ: a 1024-bin shared
 // histogram of the next 10 bits of the keys sharing the prefix found so far
-// gives the digit that holds the wanted rank.  Once no more keys share the
-// prefix than the group has threads, they are gathered, one per thread, and
-// the key of the wanted rank is read off by comparing every pair.  Ordered
-// scans over contiguous index segments then keep every candidate above tau,
-// the lowest-index ones equal to it, and the two forced pages, in ascending
-// order.
+// gives the digit that holds the wanted rank (one warp scans the bins).  Once
+// no more keys share the prefix than the group has threads, they are
+// gathered, one per thread, and the key of the wanted rank is read off by
+// comparing every pair.  One scan over contiguous index segments of the
+// candidates above tau and equal to tau then gives every thread its output
+// position: kept are the candidates above tau, the lowest-index ones equal to
+// it up to the quota, and the two forced pages, in ascending order.  The
+// sequence of group barriers is the latency of the selection, so it is kept
+// short (seven for one histogram pass).
 template <class Grp>
 __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u, const UnitPlan &s, float *sc,
                                    SelScratch &x) {
     uint32_t *keys = reinterpret_cast<uint32_t *>(sc);
     constexpr int NT = Grp::warps * 32;
-    constexpr int BPT = kSelBins / NT;   // histogram bins per thread (NT <= 1024)
-    static_assert(kSelBins % NT == 0, "bins split evenly over the group");
+    constexpr int BPL = kSelBins / 32;   // histogram bins per lane of the scanning warp
     const int tid = grp.tid, lane = grp.lane(), warp = grp.warp();
     const int N = s.N, k = s.k;
     int32_t *selrow = p.selected + (size_t)u * p.max_budget;
@@ -569,14 +594,17 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
         for (int j = tid; j < p.max_budget; j += NT) selrow[j] = j == 0 ? 0 : (j == 1 ? last : -1);
         return;
     }
-    // contiguous index segment of this thread; keys in place of the scores
+    // contiguous index segment of this thread; candidates [c0, c1) in it
     const int E = (N + NT - 1) / NT;
     const int i0 = min(N, tid * E), i1 = min(N, i0 + E);
+    const int c0 = max(i0, 1), c1 = min(i1, N - 1);
+    for (int i = tid; i < kSelBins; i += NT) x.hist[i] = 0;
+    if (tid == 0) x.gathered = 0;
     uint32_t lo = 0xffffffffu, hi = 0u;
     for (int i = i0; i < i1; ++i) {
         const uint32_t key = rank_key(sc[i]);
         keys[i] = key;
-        if (i >= 1 && i <= N - 2) { lo = min(lo, key); hi = max(hi, key); }
+        if (i >= c0 && i < c1) { lo = min(lo, key); hi = max(hi, key); }
     }
     lo = __reduce_min_sync(0xffffffffu, lo);
     hi = __reduce_max_sync(0xffffffffu, hi);
@@ -593,56 +621,66 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
         int need = kc;     // rank (1 = largest) of tau among the keys matching (prefix, pmask)
         int low = hb + 1;  // bits [low, 32) of tau are known
         int m = 0;         // keys matching the prefix
-        while (true) {
+        for (int pass = 0;; ++pass) {
             const int shift = low > 10 ? low - 10 : 0;
             const uint32_t dmask = (1u << (low - shift)) - 1u;
-            for (int i = tid; i < kSelBins; i += NT) x.hist[i] = 0;
-            grp.sync();
-            for (int i = max(i0, 1); i < min(i1, N - 1); ++i) {
+            if (pass > 0) {
+                for (int i = tid; i < kSelBins; i += NT) x.hist[i] = 0;
+                grp.sync();
+            }
+            for (int i = c0; i < c1; ++i) {
                 const uint32_t key = keys[i];
                 if ((key & pmask) == prefix) atomicAdd(&x.hist[(key >> shift) & dmask], 1);
             }
             grp.sync();
-            // thread t holds bins kSelBins-1-BPT*t .. kSelBins-BPT*(t+1) (descending digits)
-            int c[BPT], tot = 0;
+            if (warp == 0) {
+                // lane l holds the digits kSelBins-1-BPL*l down to kSelBins-BPL*(l+1)
+                const int top = kSelBins - BPL * lane;
+                int tot = 0;
 #pragma unroll
-            for (int j = 0; j < BPT; ++j) {
-                c[j] = x.hist[kSelBins - 1 - BPT * tid - j];
-                tot += c[j];
-            }
-            const int excl = group_excl_scan(grp, tot, x.warp_tot);
-            if (excl < need && need <= excl + tot) {
-                int run = excl;
+                for (int j = 0; j < BPL; j += 4) {
+                    const int4 v = *reinterpret_cast<const int4 *>(&x.hist[top - 4 - j]);
+                    tot += v.x + v.y + v.z + v.w;
+                }
+                int incl = tot;
 #pragma unroll
-                for (int j = 0; j < BPT; ++j) {
-                    if (run + c[j] >= need) {
-                        x.digit = kSelBins - 1 - BPT * tid - j;
-                        x.above = run;
-                        x.cnt = c[j];
-                        break;
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += t;
+                }
+                const int excl = incl - tot;
+                if (excl < need && need <= incl) {
+                    int run = excl;
+                    for (int j = 1; j <= BPL; ++j) {
+                        const int c = x.hist[top - j];
+                        if (run + c >= need) {
+                            x.digit = top - j;
+                            x.above = run;
+                            x.cnt = c;
+                            break;
+                        }
+                        run += c;
                     }
-                    run += c[j];
                 }
             }
             grp.sync();
-            const int dig = x.digit;
             need -= x.above;
             m = x.cnt;
-            prefix |= (uint32_t)dig << shift;
+            prefix |= (uint32_t)x.digit << shift;
             pmask |= dmask << shift;
             low = shift;
-            grp.sync();   // the scratch is reused below
             if (low == 0 || m <= NT) break;
+            grp.sync();   // every thread has read the digit before the histogram is cleared
         }
         if (low == 0) {
             tau = prefix;
         } else {
-            // gather the m <= NT keys sharing the prefix and read off rank `need`
-            int mine = 0;
-            for (int i = max(i0, 1); i < min(i1, N - 1); ++i) mine += (int)((keys[i] & pmask) == prefix);
-            int at = group_excl_scan(grp, mine, x.warp_tot);
-            for (int i = max(i0, 1); i < min(i1, N - 1); ++i)
-                if ((keys[i] & pmask) == prefix) x.list[at++] = keys[i];
+            // gather the m <= NT keys sharing the prefix (any order) and read
+            // off the key of rank `need` among them
+            for (int i = c0; i < c1; ++i) {
+                const uint32_t key = keys[i];
+                if ((key & pmask) == prefix) x.list[atomicAdd(&x.gathered, 1)] = key;
+            }
             grp.sync();
             if (tid < m) {
                 const uint32_t v = x.list[tid];
@@ -660,44 +698,27 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
     }
 
     // candidates above tau are kept; of those equal to tau, the lowest indices
-    // up to the quota: need_eq = kc - (candidates above tau)
+    // up to the quota need_eq = kc - (candidates above tau).  One scan of the
+    // packed counts (above << 16 | equal) gives both prefixes and totals.
     int gt = 0, eq = 0;
-    for (int i = max(i0, 1); i < min(i1, N - 1); ++i) {
+    for (int i = c0; i < c1; ++i) {
         gt += (int)(keys[i] > tau);
         eq += (int)(keys[i] == tau);
     }
-    const int above_before = group_excl_scan(grp, gt, x.warp_tot);
-    const int n_above = above_before + gt;   // valid in the last thread only: broadcast below
-    if (tid == NT - 1) x.above = n_above;
-    int eq_rank = group_excl_scan(grp, eq, x.warp_tot);
-    const int need_eq = kc - x.above;
-    int kept = 0;
-    {
-        int r = eq_rank;
-        for (int i = i0; i < i1; ++i) {
-            bool take;
-            if (i == 0 || i == last) take = true;
-            else {
-                const uint32_t key = keys[i];
-                take = key > tau || (key == tau && r < need_eq);
-                if (key == tau) ++r;
-            }
-            kept += take;
+    int total;
+    const int before = group_excl_scan_total(grp, (gt << 16) | eq, x.warp_tot, total);
+    const int need_eq = kc - (total >> 16);
+    int r = before & 0xffff;                            // candidates equal to tau before this segment
+    int pos = (i0 > 0 ? 1 : 0) + (before >> 16) + min(r, need_eq);
+    for (int i = i0; i < i1; ++i) {
+        bool take;
+        if (i == 0 || i == last) take = true;
+        else {
+            const uint32_t key = keys[i];
+            take = key > tau || (key == tau && r < need_eq);
+            if (key == tau) ++r;
         }
-    }
-    int pos = group_excl_scan(grp, kept, x.warp_tot);
-    {
-        int r = eq_rank;
-        for (int i = i0; i < i1; ++i) {
-            bool take;
-            if (i == 0 || i == last) take = true;
-            else {
-                const uint32_t key = keys[i];
-                take = key > tau || (key == tau && r < need_eq);
-                if (key == tau) ++r;
-            }
-            if (take && pos < p.max_budget) selrow[pos++] = i;
-        }
+        if (take && pos < p.max_budget) selrow[pos++] = i;
     }
     for (int j = k + tid; j < p.max_budget; j += NT) selrow[j] = -1;
 }
