@@ -471,17 +471,19 @@ def trace_summary(buf, qasa, sel_ctas, att_ctas, raw=False):
     nsel = qasa.TRACE_MAX_CTAS * qasa.TRACE_SELECT_EVENTS
     sel = t[:nsel].reshape(qasa.TRACE_MAX_CTAS, qasa.TRACE_SELECT_EVENTS)[:sel_ctas]
     att = t[nsel:].reshape(qasa.TRACE_MAX_CTAS, qasa.TRACE_ATTN_EVENTS)[:att_ctas]
-    ts, ta = sel[:, :3], att[:, :8]          # time stamps (the other columns hold SM ids)
+    ts, ta = sel[:, :3], np.concatenate([att[:, :8], att[:, 9:10]], axis=1)   # time stamps (not SM ids)
     rec = np.concatenate([ts[ts > 0], ta[ta > 0]])
     if rec.size == 0:
         return {}
     t0 = rec.min()
     names_s = ["start", "scored", "ids_written"]
     names_a = ["start", "prologue_done", "dependency_wait_done", "first_copy_issued", "first_page_consumed",
-               "last_copy_issued", "consumers_done", "combiner_done"]
+               "last_copy_issued", "consumers_done", "combiner_done", None, "combiner_last_states"]
     out = {}
     for pre, arr, names in (("select.", sel, names_s), ("attn.", att, names_a)):
         for j, nm in enumerate(names):
+            if nm is None:
+                continue
             v = arr[:, j]
             v = v[v > 0]
             if v.size:
@@ -494,7 +496,8 @@ def trace_summary(buf, qasa, sel_ctas, att_ctas, raw=False):
         out["raw"] = {"select_sm": sel[:, 3].tolist(), "attn_sm": att[:, 8].tolist()}
         for pre, arr, names in (("select.", sel, names_s), ("attn.", att, names_a)):
             for j, nm in enumerate(names):
-                out["raw"][pre + nm] = us(arr[:, j])
+                if nm is not None:
+                    out["raw"][pre + nm] = us(arr[:, j])
     return out
 
 

@@ -571,6 +571,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 }
                 return;
             }
+            if (pos >= n_loc && lane == 0) trace_stamp(tr ? tr + 9 : nullptr);   // the last segment's states
             // online merge over the working warps; one warp's loads are all
             // independent, so they overlap instead of forming a chain
             float acc[GMAX][JPH], Mh[GMAX], Lh[GMAX];

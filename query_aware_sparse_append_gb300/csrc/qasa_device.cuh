@@ -251,6 +251,13 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint3
         : "memory");
 }
 
+// Bulk prefetch of `bytes` contiguous bytes (16-byte aligned, a multiple of
+// 16) into L2: no register, shared memory or barrier is involved.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // Tiled 2-D TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
                                             int32_t c0, int32_t c1) {

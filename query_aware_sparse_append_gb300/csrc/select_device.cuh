@@ -149,19 +149,19 @@ __device__ void score_pages_mma(const Grp &grp, const SelectParams &p, int b, in
     const T *bounds = static_cast<const T *>(p.bounds);
     const int32_t *bt = p.block_table + (size_t)b * p.max_pages;
     // the block-table entries of a warp's next tile are loaded while its
-    // current tile's boxes are in flight (one dependent round trip per tile)
+    // current tile's boxes are in flight (one dependent round trip per tile),
+    // and the next tile's box rows are prefetched into L2 (one bulk prefetch
+    // per page row from lanes 0-15) together with the current tile's loads,
+    // so that every warp keeps two tiles on their way from HBM
+    constexpr int ROWB = 2 * D * (int)sizeof(T);
     const int tw = t_begin + warp;
     int nph0 = tw < t_end && tw * 16 + n < N ? bt[tw * 16 + n] : -1;
     int nph1 = tw < t_end && tw * 16 + n + 8 < N ? bt[tw * 16 + n + 8] : -1;
+    int pf = tw + Grp::warps < t_end && lane < 16 && (tw + Grp::warps) * 16 + lane < N
+                 ? bt[(tw + Grp::warps) * 16 + lane] : -1;
     for (int t = tw; t < t_end; t += Grp::warps) {
         const int r0 = t * 16 + n, r1 = r0 + 8;
         const int ph0 = nph0, ph1 = nph1;
-        {
-            const bool more = t + Grp::warps < t_end;
-            const int q0 = (t + Grp::warps) * 16 + n;
-            nph0 = more && q0 < N ? bt[q0] : -1;
-            nph1 = more && q0 + 8 < N ? bt[q0 + 8] : -1;
-        }
         const bool ok0 = ph0 >= 0 && ph0 < p.num_phys, ok1 = ph1 >= 0 && ph1 < p.num_phys;
         if (((r0 < N && !ok0) || (r1 < N && !ok1)) && p.status) atomicOr(p.status, QASA_DEVERR_PAGE_ID);
         const T *row0 = bounds + ((size_t)(ok0 ? ph0 : 0) * p.Hkv + h) * 2 * D;
@@ -171,6 +171,15 @@ __device__ void score_pages_mma(const Grp &grp, const SelectParams &p, int b, in
         for (int jj = 0; jj < J; ++jj) {
             a0[jj] = ok0 ? ld_global_nc_v4(row0 + (c + 4 * jj) * 8) : make_uint4(0, 0, 0, 0);
             a1[jj] = ok1 ? ld_global_nc_v4(row1 + (c + 4 * jj) * 8) : make_uint4(0, 0, 0, 0);
+        }
+        if (pf >= 0 && pf < p.num_phys) bulk_prefetch_l2(bounds + ((size_t)pf * p.Hkv + h) * 2 * D, ROWB);
+        {
+            const bool more = t + Grp::warps < t_end;
+            const int q0 = (t + Grp::warps) * 16 + n;
+            nph0 = more && q0 < N ? bt[q0] : -1;
+            nph1 = more && q0 + 8 < N ? bt[q0 + 8] : -1;
+            const int f = (t + 2 * Grp::warps) * 16 + lane;
+            pf = t + 2 * Grp::warps < t_end && lane < 16 && f < N ? bt[f] : -1;
         }
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
