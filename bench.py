@@ -709,6 +709,35 @@ def run_ours(args):
     if st:
         raise SystemExit("device errors during the benchmark: %s" % qasa.decode_device_errors(st))
 
+    # ---- the same step launched from a CUDA graph (captured once): the device
+    # time without the host's launch path between the start event and the first
+    # kernel
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step()
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=cap):
+                step()
+        torch.cuda.synchronize(dev)
+        for _ in range(3):
+            g.replay()
+        evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b_ in evg:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in evg)
+        del g
+    except Exception:   # capture refused: no graph figure
+        graph_ms = None
+
     # ---- per-kernel breakdown (same inputs, the two kernels as separate calls)
     ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
@@ -885,6 +914,9 @@ def run_ours(args):
                      "algorithmic_bytes": sel_b + att_b},
         "kernels_ms": {"select_pages": sel_ms, "sparse_attention": att_ms,
                        "select_gbs": sel_b / (sel_ms * 1e-3) / 1e9},
+        "step_graph": ({"ms_per_step": graph_ms, "queries_per_s": B / (graph_ms * 1e-3),
+                        "note": "the same step replayed from a CUDA graph (L2 flushed before each)"}
+                       if graph_ms else None),
         "step_form": "one cooperative launch (score + select + attend)" if single
                      else "two launches (select, then attention)",
         ("two_launch_step" if single else "single_launch_step"):
