@@ -99,6 +99,20 @@ def rebuild_bytes(cfg, lens):
     return int(cfg.num_kv_heads * cfg.head_dim * es * (lens.sum() + 2 * n.sum()) + 4 * n.sum())
 
 
+def append_bytes(cfg, lens):
+    """Algorithmic bytes of one decode-step append (one token per sequence and
+    KV head): the new K and V rows read and written (4*d*es), the page box read
+    and written back (4*d*es), the block-table entry and the length (8)."""
+    import numpy as np
+    es = {"f32": 4, "e4m3": 1}.get(cfg.dtype, 2)
+    ins = 4 if cfg.dtype == "f32" else 2          # appended values arrive in the input dtype
+    B = int(np.count_nonzero(np.asarray(lens) > 0))
+    per = 2 * cfg.head_dim * ins + 2 * cfg.head_dim * es + 4 * cfg.head_dim * es
+    if cfg.dtype == "e4m3":
+        per += 2 * 16                              # the page's scale record read and written
+    return int(B * cfg.num_kv_heads * per + 8 * B)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -788,6 +802,25 @@ def run_ours(args):
     # (measured on 16/32-bit caches only)
     hit = hit_rate_stats(qasa, wl, wl.budget_dev, wl.budgets, max_budget, sel) if cfg.dtype != "e4m3" else None
 
+    # ---- one decode-step append (T = 1 per sequence): every sequence's newest
+    # token written again at its own position (identical K/V, so the cache and
+    # its boxes do not change); L2 flushed before each call
+    import numpy as np
+    lens_m1 = (wl.lens_dev - 1).clamp(min=0).contiguous()
+    kl = np.stack([sq.k[max(int(L) - 1, 0):max(int(L), 1)] for sq, L in zip(wl.seqs, wl.lens)])
+    vl = np.stack([sq.v[max(int(L) - 1, 0):max(int(L), 1)] for sq, L in zip(wl.seqs, wl.lens)])
+    one_tok = (wl.lens_dev > 0).to(torch.int32).contiguous()   # empty sequences append nothing
+    k1 = paged.to_torch(kl, cfg.dtype).to(dev).contiguous()
+    v1 = paged.to_torch(vl, cfg.dtype).to(dev).contiguous()
+    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(6)]
+    for a, b_ in eva:
+        flush.zero_()
+        a.record(stream)
+        qasa.kv_append(wl.cache, wl.block_table, lens_m1, k1, v1, append_lens=one_tok, status=status)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    append_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in eva[1:])
+
     # ---- bulk rebuild of every page box from the pool (same boxes written back)
     evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
     for a, b_ in evr:
@@ -928,6 +961,10 @@ def run_ours(args):
         "page_hit_rate": hit,
         "serving_mix": (per_config or {}).get("serving_mix@125"),
         "per_config": per_config,
+        "decode_append": {"us": 1000.0 * append_ms, "bytes": append_bytes(cfg, wl.lens),
+                          "achieved_gbs": append_bytes(cfg, wl.lens) / (append_ms * 1e-3) / 1e9,
+                          "frac": append_bytes(cfg, wl.lens) / (append_ms * 1e-3) / 1e9 / peak,
+                          "note": "one new token per sequence (T = 1): launch-latency bound"},
         "metadata_rebuild": {"ms": rebuild_ms, "bytes": rebuild_b,
                              "achieved_gbs": rebuild_b / (rebuild_ms * 1e-3) / 1e9,
                              "frac": rebuild_b / (rebuild_ms * 1e-3) / 1e9 / peak},
