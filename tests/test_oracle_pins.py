@@ -390,6 +390,30 @@ def test_fp8_scale_closed_forms():
     assert np.all(np.abs(s - exact) <= 0.5 * np.spacing(s.astype(np.float32)).astype(np.float64))
 
 
+def _round_to_f32(fr):
+    """The float32 nearest to the exact rational fr (ties to the even significand)."""
+    from fractions import Fraction
+    f = np.float32(float(fr))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))]
+    return min(cands, key=lambda c: (abs(Fraction(float(c)) - fr), int(np.float32(c).view(np.uint32)) & 1))
+
+
+def test_fp8_scale_is_the_correctly_rounded_quotient():
+    # fp32 division rounds the exact quotient to nearest: compare the oracle's
+    # scale with amax / 448 computed exactly in rational arithmetic and rounded
+    # once, on random magnitudes, powers of two and values next to them
+    from fractions import Fraction
+    r = rng(45)
+    a = np.concatenate([r.random(300).astype(np.float32) * np.float32(500.0),
+                        np.exp2(np.arange(-30, 12)).astype(np.float32),
+                        np.nextafter(np.exp2(np.arange(-10, 10)).astype(np.float32), np.float32(np.inf)),
+                        np.float32([448.0, 447.99997, 1e-38, 3.4e38])])
+    got = oracle.fp8_scale(a)
+    for x, g in zip(a, got):
+        want = _round_to_f32(Fraction(float(x)) / 448)
+        assert np.float32(g).view(np.uint32) == np.float32(want).view(np.uint32), (x, g, want)
+
+
 def test_fp8_dequant_closed_forms():
     # code * scale per row: 1.0 (0x38) and -1.0 (0xB8) give +-scale, the
     # largest finite code (0x7E = 448) gives 448 * scale, zero gives 0; and a
