@@ -71,7 +71,9 @@ def barrier(device=None):
 
 def algorithmic_bytes(cfg, lens, budgets):
     """Bytes the method must move per step (and per kernel), per (sequence, KV head):
-    select:    N_b*2*d*es (page boxes) + G*d*qs (q) + 4*N_b (block table) + 4*k_b (ids out)
+    select:    N_b*2*d*es (page boxes) + G*d*qs (q) + 4*N_b (block table) + 4*k_b (ids out);
+               the first three only where some page is dropped and more than the
+               two forced pages are kept (elsewhere the kept set is fixed)
     attention: k_b*2*P*d*es (kept K and V page tiles) + 2*G*d*qs (q, out) + 8*k_b (ids, table)
     es = bytes per stored KV element, qs = bytes per query / output element.
     FP8 KV adds the page scales: 4*N_b (K amax) to the selection, 16*k_b (one
@@ -83,7 +85,9 @@ def algorithmic_bytes(cfg, lens, budgets):
     N = (np.asarray(lens, np.int64) + P - 1) // P
     k = np.minimum(N, np.maximum(np.asarray(budgets, np.int64), np.minimum(N, 2)))
     f8 = cfg.dtype == "e4m3"
-    sel = Hkv * (N * 2 * d * es + G * d * qs + 4 * N + 4 * k + (4 * N if f8 else 0))
+    # scoring (boxes, q, table) only where the scores decide the kept set
+    scored = (k < N) & (k > 2)
+    sel = Hkv * (np.where(scored, N * 2 * d * es + G * d * qs + 4 * N + (4 * N if f8 else 0), 0) + 4 * k)
     att = Hkv * (k * 2 * P * d * es + 2 * G * d * qs + 8 * k + (16 * k if f8 else 0))
     dense = Hkv * (N * 2 * P * d * es + 2 * G * d * qs + 4 * N + (16 * N if f8 else 0))
     return int(sel.sum()), int(att.sum()), int(dense.sum())

@@ -518,7 +518,9 @@ __device__ __forceinline__ UnitPlan plan_unit(const SelectParams &p, int u, bool
     const int L = valid_len(p.seq_lens[s.b], p.max_pages, p.P, rep ? p.status : nullptr);
     s.N = (L + p.P - 1) / p.P;
     s.k = kept_pages(s.N, p.budget[s.b], p.max_budget, p.status, rep);
-    s.need_scores = s.N > 0 && ((s.k < s.N) || (p.scores_out != nullptr));
+    // The scores decide the kept set only when some candidate is left out and
+    // at least one is kept beside the two forced pages (k > 2).
+    s.need_scores = s.N > 0 && ((s.k < s.N && s.k > 2) || (p.scores_out != nullptr));
     return s;
 }
 

@@ -73,6 +73,20 @@ def test_algorithmic_bytes_of_the_headline_case():
     assert dense > 5 * att
 
 
+def test_selection_bytes_only_where_scores_decide():
+    # one KV head, d 128, fp16, P 16: a unit that keeps every page (k >= N) or
+    # only the two forced pages (k = 2) reads no boxes, query or table
+    cfg = W.CONFIGS["headline_8k"]
+    P, d = cfg.page_size, cfg.head_dim
+    lens = [16 * P, 16 * P, 16 * P, 0]
+    budgets = [16, 2, 3, 5]
+    sel, att, _ = bench.algorithmic_bytes(cfg, lens, budgets)
+    H = cfg.num_kv_heads
+    scored = 16 * 2 * d * 2 + cfg.group * d * 2 + 4 * 16
+    assert sel == H * (4 * 16 + 4 * 2 + (scored + 4 * 3) + 0)
+    assert att == H * sum(k * 2 * P * d * 2 + 2 * cfg.group * d * 2 + 8 * k for k in (16, 2, 3, 0))
+
+
 def test_bench_rejects_short_warmup():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
