@@ -488,15 +488,17 @@ def trace_summary(buf, qasa, sel_ctas, att_ctas, raw=False):
     t = buf.cpu().numpy().astype(np.int64)
     nsel = qasa.TRACE_MAX_CTAS * qasa.TRACE_SELECT_EVENTS
     sel = t[:nsel].reshape(qasa.TRACE_MAX_CTAS, qasa.TRACE_SELECT_EVENTS)[:sel_ctas]
+    sel = sel[sel[:, 0] > 0]   # CTAs that ran
     att = t[nsel:].reshape(qasa.TRACE_MAX_CTAS, qasa.TRACE_ATTN_EVENTS)[:att_ctas]
-    ts, ta = sel[:, :3], np.concatenate([att[:, :8], att[:, 9:10]], axis=1)   # time stamps (not SM ids)
+    ts, ta = sel[:, :3], np.concatenate([att[:, :8], att[:, 9:11]], axis=1)   # time stamps (not SM ids)
     rec = np.concatenate([ts[ts > 0], ta[ta > 0]])
     if rec.size == 0:
         return {}
     t0 = rec.min()
     names_s = ["start", "scored", "ids_written"]
     names_a = ["start", "prologue_done", "dependency_wait_done", "first_copy_issued", "first_page_consumed",
-               "last_copy_issued", "consumers_done", "combiner_done", None, "combiner_last_states"]
+               "last_copy_issued", "consumers_done", "combiner_done", None, "combiner_last_states",
+               "combiner_last_merged", None]
     out = {}
     for pre, arr, names in (("select.", sel, names_s), ("attn.", att, names_a)):
         for j, nm in enumerate(names):
@@ -565,7 +567,7 @@ def run_trace(args):
         qasa.debug_trace(None)
         line = {"trace": cfg.name, "rep": rep, "step_us": a.elapsed_time(b_) * 1000.0,
                 "form": "one launch" if os.environ.get("QASA_SINGLE_LAUNCH") == "1" else "two launches",
-                **trace_summary(buf, qasa, min(2 * sms, qasa.TRACE_MAX_CTAS), sms, raw=args.trace_raw)}
+                **trace_summary(buf, qasa, qasa.TRACE_MAX_CTAS, sms, raw=args.trace_raw)}
         print(json.dumps(line), flush=True)
     return 0
 

@@ -381,11 +381,12 @@ int32_t qasa_host_call_is_direct(const void *q_host, const int32_t *block_table_
  * events: 0 CTA start, 1 prologue done, 2 wait for the preceding kernel done,
  * 3 first page copy issued, 4 first page consumed, 5 last page copy issued,
  * 6 last consumer warp done, 7 combiner done, 8 the SM the CTA ran on,
- * 9 the combiner has the last segment's states of every consumer warp.
+ * 9 the combiner has the last segment's states of every consumer warp,
+ * 10 the combiner has merged them, 11 unused.
  */
 #define QASA_TRACE_MAX_CTAS 4096
 #define QASA_TRACE_SELECT_EVENTS 4
-#define QASA_TRACE_ATTN_EVENTS 10
+#define QASA_TRACE_ATTN_EVENTS 12
 size_t qasa_debug_trace_bytes(void);
 qasa_status qasa_debug_trace(unsigned long long *buffer, size_t bytes);
 

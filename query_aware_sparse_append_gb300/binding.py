@@ -94,7 +94,7 @@ EXPORTED = ("qasa_kv_append", "qasa_decode_workspace_size", "qasa_select_pages",
 # trace buffer layout (include/qasa.h)
 TRACE_MAX_CTAS = 4096
 TRACE_SELECT_EVENTS = 4
-TRACE_ATTN_EVENTS = 10
+TRACE_ATTN_EVENTS = 12
 
 
 class QasaError(RuntimeError):

@@ -597,6 +597,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused
+            if (pos >= n_loc && lane == 0) trace_stamp(tr ? tr + 10 : nullptr);
             ++kseg;
 
             MT *ob = static_cast<MT *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;

@@ -29,10 +29,10 @@
 //  * FFMA (fp32 KV): a warp scores a few pages at a time with 16-byte loads
 //    and shuffle reductions.
 //
-// Selection: radix select (4 passes of 8 bits, warp-aggregated shared-memory
-// histograms) finds the key of the (k-2)-th best candidate; an ordered group
-// scan then keeps every candidate above it and the lowest-index ones equal to
-// it, and compacts the kept ids in ascending order.
+// Selection: the key of the (k-2)-th best candidate is narrowed down by
+// shared-memory histograms of 10-bit digits (usually one pass); an ordered
+// group scan then keeps every candidate above it and the lowest-index ones
+// equal to it, and compacts the kept ids in ascending order.
 #pragma once
 
 #include "qasa_device.cuh"
@@ -592,8 +592,10 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
         for (int j = tid; j < p.max_budget; j += NT) selrow[j] = -1;
         return;
     }
-    if (s.need_scores && p.scores_out)
+    if (s.need_scores && p.scores_out) {
         for (int i = tid; i < N; i += NT) p.scores_out[(size_t)u * p.max_pages + i] = sc[i];
+        grp.sync();   // the scores are read before the keys overwrite them in place
+    }
     if (k >= N) {
         for (int j = tid; j < p.max_budget; j += NT) selrow[j] = j < N ? j : -1;
         return;
