@@ -497,8 +497,8 @@ def trace_summary(buf, qasa, sel_ctas, att_ctas, raw=False):
     t0 = rec.min()
     names_s = ["start", "scored", "ids_written"]
     names_a = ["start", "prologue_done", "dependency_wait_done", "first_copy_issued", "first_page_consumed",
-               "last_copy_issued", "consumers_done", "combiner_done", None, "combiner_last_states",
-               "combiner_last_merged", None]
+               "last_copy_issued", "consumers_done", "combiner_done", None, "last_states",
+               "last_merged", None]
     out = {}
     for pre, arr, names in (("select.", sel, names_s), ("attn.", att, names_a)):
         for j, nm in enumerate(names):

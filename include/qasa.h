@@ -381,8 +381,8 @@ int32_t qasa_host_call_is_direct(const void *q_host, const int32_t *block_table_
  * events: 0 CTA start, 1 prologue done, 2 wait for the preceding kernel done,
  * 3 first page copy issued, 4 first page consumed, 5 last page copy issued,
  * 6 last consumer warp done, 7 combiner done, 8 the SM the CTA ran on,
- * 9 the combiner has the last segment's states of every consumer warp,
- * 10 the combiner has merged them, 11 unused.
+ * 9 the states of the range's last segment (when it is a whole unit) are all
+ * in shared memory, 10 that segment merged and written, 11 unused.
  */
 #define QASA_TRACE_MAX_CTAS 4096
 #define QASA_TRACE_SELECT_EVENTS 4

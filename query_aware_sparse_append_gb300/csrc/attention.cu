@@ -26,7 +26,9 @@
 // NWK working warps consume the pages (page i of the range goes to warp
 // i % NWK and stage i % S, S a multiple of NWK, so a stage is only ever used by
 // one warp); the last warp merges the working warps' softmax states at every
-// unit boundary and writes the output or the partial.  For 16-bit and FP8 KV
+// unit boundary and writes the output or the partial, while the working warps
+// go on.  Nothing follows the range's last segment, so when it is a whole unit
+// the working warps merge it themselves, a few heads each.  For 16-bit and FP8 KV
 // (any group size) a consumer computes S^T = K q^T and O^T += V^T P^T as m16n8k16
 // tensor-core MMAs (16 tokens x 8
 // query heads per MMA; ldmatrix reads the swizzled tiles conflict-free;
@@ -154,8 +156,10 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         (reinterpret_cast<uintptr_t>(sel_bar + (FUSED && MMA ? kSelStageSlots : 0)) + 1023) & ~uintptr_t(1023));
     __shared__ int s_abort;      // a bounded wait gave up
     // segment hand-off: [0] completes when the NWK working warps have written
-    // their states for a segment; [1] completes when the combiner has read them
-    __shared__ __align__(8) uint64_t seg_bar[2];
+    // their states for a segment; [1] completes when the combiner has read them;
+    // [2] completes when they have written their states for the range's last
+    // segment, if that is a whole unit (merged by the working warps themselves)
+    __shared__ __align__(8) uint64_t seg_bar[3];
     volatile int *abort_flag = &s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -179,6 +183,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             s_abort = 0;
             mbar_init(&seg_bar[0], (uint32_t)NWK);
             mbar_init(&seg_bar[1], 1);
+            mbar_init(&seg_bar[2], (uint32_t)NWK);
         }
         if constexpr (FUSED && MMA)
             for (int i = lane; i < kSelStageSlots; i += 32) mbar_init(&sel_bar[i], 1);
@@ -564,6 +569,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             const long long s1 = min(run_end(pos), ue);
             pos += s1 - g;
             const int u = b * Hkv + h;
+            if (pos >= n_loc && g == us && s1 == ue) return;   // merged by the working warps
             if (!mbar_wait_bounded(&seg_bar[0], kseg & 1u, p.wait_limit_ns)) {
                 if (lane == 0) {
                     if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
@@ -571,7 +577,6 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 }
                 return;
             }
-            if (pos >= n_loc && lane == 0) trace_stamp(tr ? tr + 9 : nullptr);   // the last segment's states
             // online merge over the working warps; one warp's loads are all
             // independent, so they overlap instead of forming a chain
             float acc[GMAX][JPH], Mh[GMAX], Lh[GMAX];
@@ -597,7 +602,6 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused
-            if (pos >= n_loc && lane == 0) trace_stamp(tr ? tr + 10 : nullptr);
             ++kseg;
 
             MT *ob = static_cast<MT *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
@@ -1020,6 +1024,38 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             }
         }
         __syncwarp();
+        if (lastx >= n_loc && g == us && s1 == ue) {
+            // The range's last segment is a whole unit: instead of handing it
+            // to the combiner (one warp merging every head), the working warps
+            // merge it together, warp w taking heads w, w + NWK, ...
+            if (lane == 0) mbar_arrive(&seg_bar[2]);
+            if (!mbar_wait_bounded(&seg_bar[2], 0u, p.wait_limit_ns)) {
+                if (lane == 0) {
+                    if (p.status) atomicOr(p.status, QASA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            if (w == 0 && lane == 0) trace_stamp(tr ? tr + 9 : nullptr);
+            constexpr int JPH = D / 32;
+            MT *ob = static_cast<MT *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+            for (int hh = w; hh < G; hh += NWK) {
+                float M = -INFINITY, L = 0.f, acc[JPH];
+#pragma unroll
+                for (int jj = 0; jj < JPH; ++jj) acc[jj] = 0.f;
+                for (int x = 0; x < NWK; ++x) {
+                    float ox[JPH];
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) ox[jj] = scr_o[(x * GMAX + hh) * D + jj * 32 + lane];
+                    merge_state<JPH>(M, L, acc, scr_m[x * GMAX + hh], scr_l[x * GMAX + hh], ox);
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<MT>::from_f(acc[jj] * inv);
+            }
+            if (w == 0 && lane == 0) trace_stamp(tr ? tr + 10 : nullptr);
+            break;
+        }
         if (lane == 0) mbar_arrive(&seg_bar[0]);
         ++kseg;
         pos = lastx;
