@@ -248,10 +248,6 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         }
     }
 
-    if (tid == 0) trace_stamp(tr ? tr + 1 : nullptr);
-    pdl_wait();   // selected ids and counters come from the preceding kernel
-    if (tid == 0) trace_stamp(tr ? tr + 2 : nullptr);
-
     // locate flattened index g: sequence b, KV head h, position j in the unit
     auto locate = [&](long long g, int &b, int &h, int &j, long long &ustart, int &cnt) {
         int lo = 0, hi = p.B - 1;
@@ -282,6 +278,35 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     const long long nL = g1 - gL;
     auto rot = [&](long long pos) -> long long { return pos < nL ? gL + pos : g0 + (pos - nL); };
     auto run_end = [&](long long pos) -> long long { return pos < nL ? g1 : gL; };
+
+    // Producer lookups (see the producer below).  Where the pages of its first
+    // two batches sit in the flattened order depends only on this kernel's
+    // inputs, so the producer works it out before waiting for the selection.
+    struct Look { int page, phys, b, h, j, stage; bool active, ok; };
+    const int WB = S < 32 ? S : 32;
+    auto look_loc = [&](long long bb, Look &lk) {   // locate; the kept id is not read yet
+        const long long pos = bb + lane;
+        lk.active = lane < WB && pos < n_loc;
+        lk.ok = false;
+        lk.page = -1; lk.phys = -1; lk.b = 0; lk.h = 0; lk.j = 0;
+        lk.stage = 2;
+        if (lk.active) {
+            int cnt;
+            long long us;
+            locate(rot(pos), lk.b, lk.h, lk.j, us, cnt);
+            lk.stage = 0;
+        }
+    };
+    Look la, lb, lc;
+    if (warp == 0) {
+        look_loc(0, la);
+        look_loc(WB, lb);
+    }
+
+    if (tid == 0) trace_stamp(tr ? tr + 1 : nullptr);
+    pdl_wait();   // selected ids and counters come from the preceding kernel
+    if (tid == 0) trace_stamp(tr ? tr + 2 : nullptr);
+
 
     if constexpr (FUSED) {
         // -------------------------------------------------------- selectors
@@ -351,7 +376,6 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         // page each (kept id -> block table -> tile row), then every lane issues
         // its own page's two TMA boxes as soon as its stage is free, so up to 32
         // copies leave per warp instruction instead of one.
-        const int WB = S < 32 ? S : 32;
         uint32_t stage0 = 0, phase0 = 0;     // stage and phase of the batch's first page
         bool aborted = false;
         // Lookups are software-pipelined over batches: the kept-id load of batch
@@ -360,7 +384,6 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         // A lookup moves through stages: 0 located, kept id not read yet (the
         // single-launch kernel reads it only once the unit's selection is
         // published); 1 id read; 2 block-table entry read, or nothing to do.
-        struct Look { int page, phys, b, h, j, stage; bool active, ok; };
         int seen_ready = -1;   // the last unit this lane saw published (acquired once)
         auto read_id = [&](Look &lk) {                   // stage 0 -> 1 when the id is available
             const size_t u = (size_t)lk.b * Hkv + lk.h;
@@ -378,18 +401,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             lk.stage = 1;
         };
         auto look_a = [&](long long bb, Look &lk) {      // locate; read the kept id
-            const long long pos = bb + lane;
-            lk.active = lane < WB && pos < n_loc;
-            lk.ok = false;
-            lk.page = -1; lk.phys = -1; lk.b = 0; lk.h = 0; lk.j = 0;
-            lk.stage = 2;
-            if (lk.active) {
-                int cnt;
-                long long us;
-                locate(rot(pos), lk.b, lk.h, lk.j, us, cnt);
-                lk.stage = 0;
-                read_id(lk);
-            }
+            look_loc(bb, lk);
+            if (lk.stage == 0) read_id(lk);
         };
         auto look_b = [&](Look &lk) {                    // check the id; read the block-table entry
             if (lk.stage == 0) read_id(lk);
@@ -430,10 +443,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             look_b(lk);
             return true;
         };
-        Look la, lb, lc;
-        look_a(0, la);
-        look_b(la);
-        look_a(WB, lb);
+        look_b(la);                                  // batches 0 and 1 were located before the wait
+        if (lb.stage == 0) read_id(lb);
         for (long long base = 0; base < n_loc && !aborted; base += WB) {
             const int nb = (int)min((long long)WB, n_loc - base);
             if (!finish(la)) {
