@@ -25,10 +25,10 @@
 // map is refused) into a ring of shared-memory stages guarded by mbarriers.
 // NWK working warps consume the pages (page i of the range goes to warp
 // i % NWK and stage i % S, S a multiple of NWK, so a stage is only ever used by
-// one warp); the last warp merges the working warps' softmax states at every
-// unit boundary and writes the output or the partial, while the working warps
-// go on.  Nothing follows the range's last segment, so when it is a whole unit
-// the working warps merge it themselves, a few heads each.  For 16-bit and FP8 KV
+// one warp); the remaining warps merge the working warps' softmax states at
+// every unit boundary (a few heads each) and write the output or the partial,
+// while the working warps go on.  Nothing follows the range's last segment, so
+// when it is a whole unit the working warps merge it themselves.  For 16-bit and FP8 KV
 // (any group size) a consumer computes S^T = K q^T and O^T += V^T P^T as m16n8k16
 // tensor-core MMAs (16 tokens x 8
 // query heads per MMA; ldmatrix reads the swizzled tiles conflict-free;
@@ -156,7 +156,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         (reinterpret_cast<uintptr_t>(sel_bar + (FUSED && MMA ? kSelStageSlots : 0)) + 1023) & ~uintptr_t(1023));
     __shared__ int s_abort;      // a bounded wait gave up
     // segment hand-off: [0] completes when the NWK working warps have written
-    // their states for a segment; [1] completes when the combiner has read them;
+    // their states for a segment; [1] completes when the combiners have read them;
     // [2] completes when they have written their states for the range's last
     // segment, if that is a whole unit (merged by the working warps themselves)
     __shared__ __align__(8) uint64_t seg_bar[3];
@@ -182,7 +182,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         if (lane == 0) {
             s_abort = 0;
             mbar_init(&seg_bar[0], (uint32_t)NWK);
-            mbar_init(&seg_bar[1], 1);
+            mbar_init(&seg_bar[1], (uint32_t)(NW - NWK));
             mbar_init(&seg_bar[2], (uint32_t)NWK);
         }
         if constexpr (FUSED && MMA)
@@ -553,7 +553,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     }
 
     // A working warp may overwrite the shared state slot for segment k once the
-    // combiner has read segment k-1 (phase k-1 of the "free" barrier).
+    // combiners have read segment k-1 (phase k-1 of the "free" barrier).
     auto wait_slot_free = [&](uint32_t k) -> bool {
         if (mbar_wait_bounded(&seg_bar[1], (k & 1u) ^ 1u, p.wait_limit_ns)) return true;
         if (lane == 0) {
@@ -563,11 +563,17 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         return false;
     };
 
-    // The combiner: for every segment of the CTA range, in order, merge the
+    // The combiners: for every segment of the CTA range, in order, merge the
     // working warps' (m, l, o) into registers, release the slot, then write the
     // output (whole unit) or this CTA's partial plus the unit's page ticket; the
     // CTA that completes a unit's ticket merges all its partials.
-    auto combine_segments = [&]() {
+    //
+    // The warps not working on pages (NC = NW - NWK >= 1 of them, index ci)
+    // share this: a whole unit's heads are split between them (heads ci,
+    // ci + NC, ...); a unit split with another CTA is done by warp 0 of them
+    // alone (all heads, the partial, the ticket and the last merge) while the
+    // others only release the slot.
+    auto combine_segments = [&](int ci, int NC) {
         constexpr int JPH = D / 32;                    // elements per lane per head
         long long pos = 0;
         uint32_t kseg = 0;
@@ -588,6 +594,50 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 }
                 return;
             }
+            const bool whole = g == us && s1 == ue;    // the whole unit is in this CTA
+            if (whole && NC > 1) {
+                // heads ci, ci + NC, ... (at most KH of them) of a whole unit
+                constexpr int KH = (GMAX + 1) / 2;
+                float acc[KH][JPH], Mh[KH], Lh[KH];
+#pragma unroll
+                for (int k = 0; k < KH; ++k) {
+                    Mh[k] = -INFINITY;
+                    Lh[k] = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) acc[k][jj] = 0.f;
+                }
+                for (int x = 0; x < NWK; ++x) {
+#pragma unroll
+                    for (int k = 0; k < KH; ++k) {
+                        const int hh = ci + k * NC;
+                        if (hh >= G) break;
+                        float ox[JPH];
+#pragma unroll
+                        for (int jj = 0; jj < JPH; ++jj) ox[jj] = scr_o[(x * GMAX + hh) * D + jj * 32 + lane];
+                        merge_state<JPH>(Mh[k], Lh[k], acc[k], scr_m[x * GMAX + hh], scr_l[x * GMAX + hh], ox);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused (once every combiner is here)
+                ++kseg;
+                MT *ob = static_cast<MT *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
+#pragma unroll
+                for (int k = 0; k < KH; ++k) {
+                    const int hh = ci + k * NC;
+                    if (hh >= G) break;
+                    const float inv = Lh[k] > 0.f ? 1.f / Lh[k] : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < JPH; ++jj) ob[hh * D + jj * 32 + lane] = elem<MT>::from_f(acc[k][jj] * inv);
+                }
+                continue;
+            }
+            if (!whole && ci != 0) {                   // warp 0 of the combiners takes it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&seg_bar[1]);
+                ++kseg;
+                continue;
+            }
+            // every head (a whole unit with one combiner warp, or a split unit):
             // online merge over the working warps; one warp's loads are all
             // independent, so they overlap instead of forming a chain
             float acc[GMAX][JPH], Mh[GMAX], Lh[GMAX];
@@ -612,11 +662,11 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 for (int hh = 0; hh < GMAX; ++hh) merge_state<JPH>(Mh[hh], Lh[hh], acc[hh], mx[hh], lx[hh], ox[hh]);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused
+            if (lane == 0) mbar_arrive(&seg_bar[1]);   // the slot may be reused (once every combiner is here)
             ++kseg;
 
             MT *ob = static_cast<MT *>(p.out) + ((size_t)b * p.Hq + (size_t)h * G) * D;
-            if (g == us && s1 == ue) {                  // the whole unit is in this CTA
+            if (whole) {
 #pragma unroll
                 for (int hh = 0; hh < GMAX; ++hh) {
                     if (hh >= G) break;
@@ -687,16 +737,15 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     };
 
     // ---------------------------------------------------------------- consumers
-    // Warps 1..NWK take pages; the last warp is the combiner, which merges the
-    // working warps' states at every unit boundary (segment) of the CTA range
-    // while they move on; any other warp has nothing to do.
+    // Warps 1..NWK take pages; the other warps are the combiners, which merge
+    // the working warps' states at every unit boundary (segment) of the CTA
+    // range while they move on.
     const int w = warp - 1;
-    if (w == NW - 1) {
-        combine_segments();
-        if (lane == 0) trace_stamp(tr ? tr + 7 : nullptr);
+    if (w >= NWK) {
+        combine_segments(w - NWK, NW - NWK);
+        if (w == NW - 1 && lane == 0) trace_stamp(tr ? tr + 7 : nullptr);
         return;
     }
-    if (w >= NWK) return;
     long long pos = 0;
     uint32_t kseg = 0;
     while (pos < n_loc) {
@@ -898,7 +947,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                 __syncwarp();
                 if (!F8CONV && lane == 0) mbar_arrive(&empty_bar[s]);
             }
-            // hand this warp's state to the combiner
+            // hand this warp's state to the combiners
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -1037,7 +1086,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         __syncwarp();
         if (lastx >= n_loc && g == us && s1 == ue) {
             // The range's last segment is a whole unit: instead of handing it
-            // to the combiner (one warp merging every head), the working warps
+            // to the combiners (a few warps), the working warps
             // merge it together, warp w taking heads w, w + NWK, ...
             if (lane == 0) mbar_arrive(&seg_bar[2]);
             if (!mbar_wait_bounded(&seg_bar[2], 0u, p.wait_limit_ns)) {
@@ -1108,7 +1157,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
             if (s >= 4 * kPreferred) { stages = s; consumers = kPreferred; }
         }
     }
-    for (int nw = NW - 1; nw >= 1 && stages == 0; --nw) {   // the last consumer warp is the combiner
+    for (int nw = NW - 1; nw >= 1 && stages == 0; --nw) {   // at least one warp is left to combine
         const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);
