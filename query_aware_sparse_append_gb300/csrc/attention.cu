@@ -1145,9 +1145,10 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     int stages = 0, consumers = 0;
     // 16-bit KV: four working warps whenever the ring still holds at least four
     // pages per warp (fewer states per unit-boundary merge; the streaming rate
-    // is the same from four warps up)
+    // is the same from four warps up), six for pages of 4 KB or less, whose
+    // rate is set by the per-page work rather than by the bytes
     if constexpr (!F8) {
-        constexpr int kPreferred = 4;
+        constexpr int kPreferred = STAGE <= 4096 ? 6 : 4;
         if (kPreferred <= NW - 1) {
             const size_t fixed = attn_smem_bytes(0, STAGE, kPreferred, GMAX, D, P, MMA, p.B, FUSED, p.max_pages,
                                                  F8, F8CONV);
