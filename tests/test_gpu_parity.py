@@ -304,3 +304,14 @@ def test_separate_kv_boxes_give_the_same_result(name, batch, seed, env, monkeypa
     assert st1 == 0 and st2 == 0
     assert torch.equal(s1, s2)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_zz_fp32_clause_decides_few_units():
+    # The selection checks of this session (this module and the ones before
+    # it): units whose sets differ beyond the 1e-5 relative tie rule, admitted
+    # only by the fp32 summation bounds of the pages involved, must stay rare,
+    # so that a looser comparison cannot hide a ranking error.
+    st = H.SEL_STATS
+    if st["units"] == 0:
+        pytest.skip("no selection was checked")
+    assert st["fp32_band"] <= max(2, st["units"] // 100), st
