@@ -17,6 +17,7 @@ namespace {
 constexpr int kMaxPagesPerSeq = 16384;
 constexpr int kMaxBatch = 8192;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
+constexpr int kAttnUnitWeight = 4;
 
 // Limit of the waits on other warps, CTAs and flags.  QASA_WAIT_LIMIT_NS
 // (diagnostic, for tests of the time-out path) shortens it, down to 1 us; the
@@ -27,6 +28,22 @@ unsigned long long wait_limit_ns() {
     const unsigned long long n = std::strtoull(v, nullptr, 10);
     if (n < 1000ull) return 1000ull;
     return n < kWaitLimitNs ? n : kWaitLimitNs;
+}
+
+// Page-equivalents of work a unit adds to an attention CTA's range (its query
+// load, the hand-over of the working warps' states and their merge): ranges
+// balance pages plus this per unit, so that a range of many short units gets
+// fewer pages.  The cost is about fixed in time, so it is worth more of the
+// smaller pages: 4 pages of 8 KiB (K + V), 8 of 4 KiB, 2 of 16 KiB (measured
+// best or level on the workloads of each size).  QASA_ATTN_UNIT_WEIGHT
+// (diagnostic) overrides it, 0 .. 256.
+int attn_unit_weight(size_t page_kv_bytes) {
+    if (const char *v = std::getenv("QASA_ATTN_UNIT_WEIGHT")) {
+        const long n = std::strtol(v, nullptr, 10);
+        return n < 0 ? 0 : n > 256 ? 256 : (int)n;
+    }
+    const size_t w = (size_t)kAttnUnitWeight * 8192 / (page_kv_bytes ? page_kv_bytes : 1);
+    return w < 1 ? 1 : w > 16 ? 16 : (int)w;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -332,6 +349,7 @@ qasa_status run_attention(const qasa_kv_cache *cache, const void *q, int num_q_h
     const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)cache->head_dim);
     p.scale_log2 = (float)(sc * 1.4426950408889634);
     p.dense = dense ? 1 : 0;
+    p.unit_weight = attn_unit_weight(2 * (size_t)cache->page_size * cache->head_dim * elem_size(cache->dtype));
     p.one_box = one_box;
     p.stages = 0;
     p.consumers = 0;

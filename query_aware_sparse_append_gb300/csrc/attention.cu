@@ -59,7 +59,7 @@ constexpr int kSelSlotsPerWarp = 2;                    // box tiles in flight pe
 constexpr int kSelStageSlots = 4 * kSelSlotsPerWarp;
 
 // Host-side size of the dynamic shared memory (mirrors the device carve-up).
-size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int P, bool mma, int B,
+size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int P, bool mma, int B, int grid,
                        bool fused, int max_pages, bool fp8 = false, bool fp8_scratch = false) {
     size_t s = 1024;                                   // alignment slack for the ring
     s += (size_t)stages * stage_bytes;
@@ -70,6 +70,7 @@ size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int
     s += (size_t)nw * gmax * (D + 2) * sizeof(float);  // combine scratch
     if (!mma) s += (size_t)nw * gmax * (D + P) * sizeof(float);
     s += (size_t)(2 * B + 2) * sizeof(int);            // prefix, lengths
+    s += 8 + (size_t)(grid + 1) * sizeof(long long);   // every CTA's first page
     if (fused) {
         // selector scratch: scores, block-table row, box staging slots + barriers
         s += 16 + (size_t)max_pages * sizeof(float) + 16 + sizeof(SelScratch);
@@ -80,12 +81,13 @@ size_t attn_smem_bytes(int stages, int stage_bytes, int nw, int gmax, int D, int
     return s;
 }
 
-__device__ __forceinline__ long long range_start(int c, int C, long long T) {
-    return (long long)c * T / C;
-}
-// CTA whose range holds flattened index g (0 <= g < T).
-__device__ __forceinline__ int cta_of(long long g, int C, long long T) {
-    return (int)(((g + 1) * C - 1) / T);
+// CTA ranges are balanced on weighted work: the flattened page g of unit u
+// (unit-major order) sits at v(g) = g + W0 * (u + 1), so that every unit adds
+// W0 page-equivalents (its query, its state hand-over and merge) before its
+// pages; CTA c of C takes the pages with v in [c*V/C, (c+1)*V/C), V = T + W0*U.
+// CTA whose range holds the page at weighted position v (0 <= v < V).
+__device__ __forceinline__ int cta_of_v(long long v, int C, long long V) {
+    return (int)(((v + 1) * C - 1) / V);
 }
 
 // Online merge of one softmax state (m, l, o[]) into a running one (log2 domain).
@@ -137,10 +139,12 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     float *ff_p = ff_q + (MMA ? 0 : NWK * GMAX * D);               // FFMA only: [NWK][GMAX][P]
     int *prefix = reinterpret_cast<int *>(ff_p + (MMA ? 0 : NWK * GMAX * P));  // [B + 1]
     int *lens = prefix + (p.B + 1);                                // [B]
+    long long *rstart = reinterpret_cast<long long *>(                 // [C + 1] every CTA's first page
+        (reinterpret_cast<uintptr_t>(lens + p.B) + 7) & ~uintptr_t(7));
     // single launch: the selector warps' scores [max_pages], scratch, the
     // unit's block-table row [max_pages] and (tensor-core scoring) the box
     // staging slots with their barriers
-    float *sel_sc = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(lens + p.B) + 15) & ~uintptr_t(15));
+    float *sel_sc = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(rstart + gridDim.x + 1) + 15) & ~uintptr_t(15));
     SelScratch *sel_x = reinterpret_cast<SelScratch *>(
         (reinterpret_cast<uintptr_t>(sel_sc + (FUSED ? p.max_pages : 0)) + 15) & ~uintptr_t(15));
     int32_t *sel_phys = reinterpret_cast<int32_t *>(
@@ -230,7 +234,34 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
         any_empty = __syncthreads_or(any_empty);
     }
     const long long Ttot = (long long)Hkv * prefix[p.B];
-    const long long g0 = range_start(c, C, Ttot), g1 = range_start(c + 1, C, Ttot);
+    // (the weight and the weighted total are recomputed from the parameters
+    // where they are used rather than held in registers across the kernel)
+    auto unit_w = [&]() -> long long { return p.dense ? 0 : p.unit_weight; };
+    auto weighted_total = [&]() -> long long { return (long long)Hkv * prefix[p.B] + unit_w() * (p.B * Hkv); };
+    // first page of CTA cc's range: the first page whose weighted position
+    // reaches cc*V/C (the first unit that ends past it, then the page in it)
+    auto range_start = [&](int cc) -> long long {
+        const int U = p.B * Hkv;
+        const long long W0 = unit_w();
+        if (cc >= C) return (long long)Hkv * prefix[p.B];
+        const long long V = (long long)cc * weighted_total() / C;
+        int lo = 0, hi = U;
+        while (lo < hi) {   // first unit u with ue(u) + W0 (u + 1) > V
+            const int mid = (lo + hi) >> 1;
+            const int bb = mid / Hkv, hh = mid - bb * Hkv;
+            const int cn = prefix[bb + 1] - prefix[bb];
+            const long long ue = (long long)Hkv * prefix[bb] + (long long)(hh + 1) * cn;
+            if (ue + W0 * (mid + 1) > V) hi = mid; else lo = mid + 1;
+        }
+        if (lo >= U) return (long long)Hkv * prefix[p.B];
+        const int bb = lo / Hkv, hh = lo - bb * Hkv;
+        const long long us = (long long)Hkv * prefix[bb] + (long long)hh * (prefix[bb + 1] - prefix[bb]);
+        const long long g = V - W0 * (lo + 1);
+        return g > us ? g : us;
+    };
+    for (int x = tid; x <= C; x += blockDim.x) rstart[x] = range_start(x);
+    __syncthreads();
+    const long long g0 = rstart[c], g1 = rstart[c + 1];
 
     // sequences with no pages: zero their outputs (unit u handled by CTA u % C)
     if (any_empty) {
@@ -701,7 +732,8 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
             last = __shfl_sync(0xffffffffu, last, 0);
             __syncwarp();
             if (last) {
-                const int cf = cta_of(us, C, Ttot), cl = cta_of(ue - 1, C, Ttot);
+                const long long wu = unit_w() * (u + 1), vt = weighted_total();
+                const int cf = cta_of_v(us + wu, C, vt), cl = cta_of_v(ue - 1 + wu, C, vt);
 #pragma unroll
                 for (int hh = 0; hh < GMAX; ++hh) {
                     Mh[hh] = -INFINITY;
@@ -710,7 +742,7 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
                     for (int jj = 0; jj < JPH; ++jj) acc[hh][jj] = 0.f;
                 }
                 for (int x = cf; x <= cl; ++x) {
-                    if (range_start(x, C, Ttot) == range_start(x + 1, C, Ttot)) continue;   // empty range
+                    if (rstart[x] == rstart[x + 1]) continue;   // empty range
                     const size_t sb = (size_t)(u + x) * G;
                     float mx[GMAX], lx[GMAX], ox[GMAX][JPH];
 #pragma unroll
@@ -1150,7 +1182,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     if constexpr (!F8) {
         constexpr int kPreferred = STAGE <= 4096 ? 6 : 4;
         if (kPreferred <= NW - 1) {
-            const size_t fixed = attn_smem_bytes(0, STAGE, kPreferred, GMAX, D, P, MMA, p.B, FUSED, p.max_pages,
+            const size_t fixed = attn_smem_bytes(0, STAGE, kPreferred, GMAX, D, P, MMA, p.B, grid, FUSED, p.max_pages,
                                                  F8, F8CONV);
             int s = fixed < smem_budget ? (int)((smem_budget - fixed) / per) : 0;
             if (s > kMaxStages) s = kMaxStages;
@@ -1159,7 +1191,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
         }
     }
     for (int nw = NW - 1; nw >= 1 && stages == 0; --nw) {   // at least one warp is left to combine
-        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
+        const size_t fixed = attn_smem_bytes(0, STAGE, nw, GMAX, D, P, MMA, p.B, grid, FUSED, p.max_pages, F8, F8CONV);
         if (fixed >= smem_budget) continue;
         int s = (int)((smem_budget - fixed) / per);
         if (s > kMaxStages) s = kMaxStages;
@@ -1178,7 +1210,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     if (const char *force = std::getenv("QASA_ATTN_CONSUMERS")) {   // diagnostic: fix the consumer warps
         const int want = std::atoi(force);
         if (want >= 1 && want <= NW - 1) {
-            const size_t fixed = attn_smem_bytes(0, STAGE, want, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
+            const size_t fixed = attn_smem_bytes(0, STAGE, want, GMAX, D, P, MMA, p.B, grid, FUSED, p.max_pages, F8, F8CONV);
             int s = fixed < smem_budget ? (int)((smem_budget - fixed) / per) : 0;
             if (s > kMaxStages) s = kMaxStages;
             s = s / want * want;
@@ -1188,7 +1220,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &km, const CUtensorMap &vm, c
     if (stages < 2) return cudaErrorInvalidConfiguration;
     p.stages = stages;
     p.consumers = consumers;
-    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B, FUSED, p.max_pages, F8, F8CONV);
+    const size_t smem = attn_smem_bytes(stages, STAGE, consumers, GMAX, D, P, MMA, p.B, grid, FUSED, p.max_pages, F8, F8CONV);
     auto kern = attn_kernel<T, D, P, MMA, GMAX, NW, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

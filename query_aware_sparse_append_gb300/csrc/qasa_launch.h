@@ -53,6 +53,7 @@ struct AttnParams {
     int B, Hkv, G, Hq, max_pages, max_budget, num_phys;
     float scale_log2;
     int dense;
+    int unit_weight;   // page-equivalents a unit adds to a CTA range's work (ranges balance pages + this per unit)
     int one_box;       // 2: one box per page holding its K and V tiles (kmap only);
                        // 1: one 3-D TMA box per K/V tile; 0: one 2-D box per 128 bytes of head dim
     int stages;        // ring depth, a multiple of `consumers`

@@ -3,7 +3,8 @@ the library launches (1 .. SM count; small batches get fewer CTAs than SMs).
 
 The kernel flattens all kept (unit, page) pairs unit-major (unit = sequence b,
 KV head h; sequence b contributes Hkv units of cnt_b pages each), gives CTA c of
-C the range [c*T/C, (c+1)*T/C), walks it rotated (first the part of its last
+C the pages whose weighted position g + W0*(u+1) lies in [c*V/C, (c+1)*V/C),
+V = T + W0*U (every unit adds W0 page-equivalents of work), walks it rotated (first the part of its last
 unit that starts inside the range, then the rest), writes whole units directly
 and, for a unit cut by a range boundary, a partial to slot unit + c plus a page
 ticket; the CTA whose ticket completes the unit merges the partials of CTAs
@@ -28,18 +29,41 @@ import pytest
 
 
 class Split:
-    def __init__(self, cnts, Hkv, C):
-        self.B, self.Hkv, self.C, self.cnts = len(cnts), Hkv, C, cnts
+    def __init__(self, cnts, Hkv, C, W0=0):
+        self.B, self.Hkv, self.C, self.cnts, self.W0 = len(cnts), Hkv, C, cnts, W0
         self.prefix = [0]
         for x in cnts:
             self.prefix.append(self.prefix[-1] + x)
         self.T = Hkv * self.prefix[-1]
+        self.U = self.B * Hkv
+        self.V = self.T + W0 * self.U   # weighted work: pages + W0 per unit
+
+    def unit_bounds(self, u):
+        b, h = divmod(u, self.Hkv)
+        cnt = self.cnts[b]
+        us = self.Hkv * self.prefix[b] + h * cnt
+        return us, us + cnt
 
     def range_start(self, c):
-        return c * self.T // self.C
+        """First page whose weighted position g + W0*(u+1) reaches c*V/C."""
+        if c >= self.C:
+            return self.T
+        V = c * self.V // self.C
+        lo, hi = 0, self.U
+        while lo < hi:          # first unit u with ue(u) + W0*(u+1) > V
+            mid = (lo + hi) >> 1
+            if self.unit_bounds(mid)[1] + self.W0 * (mid + 1) > V:
+                hi = mid
+            else:
+                lo = mid + 1
+        if lo >= self.U:
+            return self.T
+        return max(self.unit_bounds(lo)[0], V - self.W0 * (lo + 1))
 
     def cta_of(self, g):
-        return ((g + 1) * self.C - 1) // self.T
+        b, h, _, _ = self.locate(g)
+        v = g + self.W0 * (b * self.Hkv + h + 1)
+        return ((v + 1) * self.C - 1) // self.V
 
     def locate(self, g):
         lo, hi = 0, self.B - 1
@@ -100,8 +124,8 @@ class Split:
         return sel
 
 
-def check(cnts, Hkv, C):
-    m = Split(cnts, Hkv, C)
+def check(cnts, Hkv, C, W0=0):
+    m = Split(cnts, Hkv, C, W0)
     if m.T == 0:
         return
     segs = []
@@ -166,14 +190,36 @@ def test_work_split_invariants_for_every_grid(seed):
         most = max(cnts) if max(cnts) else 2
         C = rng.choice([1, 2, 3, 5, 8, 37, 64, 151, 152,
                         attention_grid(B * Hkv, most, 152)])
-        check(cnts, Hkv, C)
+        check(cnts, Hkv, C, W0=rng.choice([0, 1, 4, 4, 9, 256]))
 
 
-def test_headline_and_small_batch_shapes():
-    check([64] * 128, 4, 152)                       # the 8K / 12.5 % headline
-    check([16], 4, attention_grid(4, 16, 152))      # one sequence: 8 CTAs
-    check([64, 64], 4, attention_grid(8, 64, 152))  # two sequences: 64 CTAs
-    check([0, 40, 0, 3, 2, 128], 4, 152)            # empty sequences and ragged budgets
+@pytest.mark.parametrize("W0", [0, 4])
+def test_headline_and_small_batch_shapes(W0):
+    check([64] * 128, 4, 152, W0)                       # the 8K / 12.5 % headline
+    check([16], 4, attention_grid(4, 16, 152), W0)      # one sequence: 8 CTAs
+    check([64, 64], 4, attention_grid(8, 64, 152), W0)  # two sequences: 64 CTAs
+    check([0, 40, 0, 3, 2, 128], 4, 152, W0)            # empty sequences and ragged budgets
+
+
+def test_unit_weight_moves_pages_away_from_ranges_of_short_units():
+    # a batch of one long sequence then many short ones: with a weight per
+    # unit, the CTAs holding the short units get fewer pages, and every CTA's
+    # pages + W0 * (units it starts) stay within one unit's worth of the mean
+    cnts = [512] + [4] * 127
+    for W0 in (0, 4):
+        m = Split(cnts, 4, 152, W0)
+        work = []
+        for c in range(152):
+            segs = m.segments(c)
+            pages = sum(s1 - g for g, s1, _, _, _ in segs)
+            starts = sum(1 for g, _, _, us, _ in segs if g == us)
+            work.append(pages + W0 * starts)
+        if W0:
+            assert max(work) - min(work) <= 512 // 152 + W0 + 2, (min(work), max(work))
+    m0, m4 = Split(cnts, 4, 152, 0), Split(cnts, 4, 152, 4)
+    last0 = sum(s1 - g for g, s1, _, _, _ in m0.segments(151))
+    last4 = sum(s1 - g for g, s1, _, _, _ in m4.segments(151))
+    assert last4 < last0   # the last CTA (all short units) gets fewer pages
 
 
 def test_small_batch_grid_bounds():
