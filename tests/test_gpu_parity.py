@@ -306,6 +306,29 @@ def test_separate_kv_boxes_give_the_same_result(name, batch, seed, env, monkeypa
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
+@pytest.mark.parametrize("name,batch", [("headline_8k", 12), ("llama_1b3_32k", 2), ("serving_mix", 24)])
+def test_repeated_steps_on_a_reused_workspace_give_identical_bits(name, batch):
+    # the workspace starts as garbage from an unrelated user; every step must
+    # read only what it (or the selection before it) wrote, so the first step
+    # and the later ones agree bit for bit (a partial read before it is
+    # written shows up here as a difference in the first step only)
+    from query_aware_sparse_append_gb300 import binding as qasa
+    case = H.make_case(W.CONFIGS[name], seed=58, batch=batch)
+    ws = qasa.alloc_workspace(case.cache, batch, case.cfg.num_q_heads, case.bt.shape[1])
+    ws.fill_(0x5A)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(4):
+        out, sel = qasa.sparse_decode_attention(case.cache, case.q_dev, case.bt, case.lens_dev, case.budget_dev,
+                                                max_budget=case.max_budget, workspace=ws, status=status)
+        outs.append((out.clone(), sel.clone()))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for out, sel in outs[1:]:
+        assert torch.equal(sel, outs[0][1])
+        assert torch.equal(out.view(torch.int16), outs[0][0].view(torch.int16))
+
+
 def test_zz_fp32_clause_decides_few_units():
     # The selection checks of this session (this module and the ones before
     # it): units whose sets differ beyond the 1e-5 relative tie rule, admitted
