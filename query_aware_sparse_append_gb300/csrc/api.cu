@@ -126,7 +126,7 @@ constexpr int kMinPagesPerCta = 8;
 // QASA_SINGLE_LAUNCH=1 asks for the single cooperative launch.  On GB300 the
 // two-kernel form is faster for every measured workload: inside one launch
 // only four warps per SM select, and a unit's selection (block-table row, box
-// scoring, radix select; ~20 us per unit, latency-bound) then paces the
+// scoring, top-k; ~20 us per unit, latency-bound) then paces the
 // attention streaming.
 bool single_launch_enabled() {
     const char *v = std::getenv("QASA_SINGLE_LAUNCH");

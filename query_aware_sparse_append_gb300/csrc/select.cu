@@ -15,7 +15,7 @@
 // head) that split its 16-page tiles evenly and store their scores straight
 // into the first CTA's shared memory (distributed shared memory), which then
 // selects; the scoring paths (tensor-core contraction through the sign split,
-// or FFMA) and the radix selection live in select_device.cuh, shared with the
+// or FFMA) and the top-k selection live in select_device.cuh, shared with the
 // single-launch decode kernel.
 #include <cstdlib>
 

@@ -175,7 +175,7 @@ def test_decode_step_append_then_attend():
 def test_selection_with_exact_ties_and_mixed_signs(name):
     # pages copied verbatim share their box, hence their score exactly: the tie
     # must go to the lower page index; pages pushed against q score negative,
-    # so the keys of one unit span both signs (every radix bit in play)
+    # so the keys of one unit span both signs (the sign bit of the keys in play)
     from query_aware_sparse_append_gb300 import paged
     cfg = W.CONFIGS[name]
     case = H.make_case(cfg, seed=31, batch=3, device=False)
