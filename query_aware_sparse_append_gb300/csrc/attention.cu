@@ -239,24 +239,27 @@ attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CU
     auto unit_w = [&]() -> long long { return p.dense ? 0 : p.unit_weight; };
     auto weighted_total = [&]() -> long long { return (long long)Hkv * prefix[p.B] + unit_w() * (p.B * Hkv); };
     // first page of CTA cc's range: the first page whose weighted position
-    // reaches cc*V/C (the first unit that ends past it, then the page in it)
+    // reaches V = cc*Vtot/C.  Sequence b's units end at weighted positions
+    // base_b + (h+1)*step_b with base_b = Hkv*(prefix[b] + W0*b) and
+    // step_b = cnt_b + W0, so: the first sequence whose last unit ends past V
+    // (a search over the sequences), then the unit in it, then the page.
     auto range_start = [&](int cc) -> long long {
-        const int U = p.B * Hkv;
         const long long W0 = unit_w();
         if (cc >= C) return (long long)Hkv * prefix[p.B];
         const long long V = (long long)cc * weighted_total() / C;
-        int lo = 0, hi = U;
-        while (lo < hi) {   // first unit u with ue(u) + W0 (u + 1) > V
+        int lo = 0, hi = p.B;
+        while (lo < hi) {   // first b with base_{b+1} > V
             const int mid = (lo + hi) >> 1;
-            const int bb = mid / Hkv, hh = mid - bb * Hkv;
-            const int cn = prefix[bb + 1] - prefix[bb];
-            const long long ue = (long long)Hkv * prefix[bb] + (long long)(hh + 1) * cn;
-            if (ue + W0 * (mid + 1) > V) hi = mid; else lo = mid + 1;
+            if ((long long)Hkv * (prefix[mid + 1] + W0 * (mid + 1)) > V) hi = mid; else lo = mid + 1;
         }
-        if (lo >= U) return (long long)Hkv * prefix[p.B];
-        const int bb = lo / Hkv, hh = lo - bb * Hkv;
-        const long long us = (long long)Hkv * prefix[bb] + (long long)hh * (prefix[bb + 1] - prefix[bb]);
-        const long long g = V - W0 * (lo + 1);
+        if (lo >= p.B) return (long long)Hkv * prefix[p.B];
+        const int cn = prefix[lo + 1] - prefix[lo];
+        const long long base = (long long)Hkv * (prefix[lo] + W0 * lo), step = cn + W0;   // step > 0 here
+        long long hh = (V - base) / step;   // units of b that end at or before V
+        if (hh < 0) hh = 0;
+        if (hh > Hkv - 1) hh = Hkv - 1;
+        const long long us = (long long)Hkv * prefix[lo] + hh * cn;
+        const long long g = V - W0 * ((long long)lo * Hkv + hh + 1);
         return g > us ? g : us;
     };
     for (int x = tid; x <= C; x += blockDim.x) rstart[x] = range_start(x);

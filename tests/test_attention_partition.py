@@ -231,3 +231,41 @@ def test_small_batch_grid_bounds():
             C = attention_grid(units, most, 152)
             assert 1 <= C <= 152
             assert C == 152 or units * most <= 8 * C
+
+
+def range_start_by_sequence(m, c):
+    """The kernel's form of range_start: a search over the sequences (their
+    last units end at weighted positions Hkv*(prefix[b+1] + W0*(b+1))), then
+    the unit inside the sequence by one division, then the page."""
+    if c >= m.C:
+        return m.T
+    V = c * m.V // m.C
+    lo, hi = 0, m.B
+    while lo < hi:
+        mid = (lo + hi) >> 1
+        if m.Hkv * (m.prefix[mid + 1] + m.W0 * (mid + 1)) > V:
+            hi = mid
+        else:
+            lo = mid + 1
+    if lo >= m.B:
+        return m.T
+    cn = m.cnts[lo]
+    base, step = m.Hkv * (m.prefix[lo] + m.W0 * lo), cn + m.W0
+    hh = min(max((V - base) // step, 0), m.Hkv - 1)
+    us = m.Hkv * m.prefix[lo] + hh * cn
+    return max(us, V - m.W0 * (lo * m.Hkv + hh + 1))
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_sequence_search_matches_the_unit_search(seed):
+    rng = random.Random(100 + seed)
+    for _ in range(1500):
+        B = rng.randint(1, 40)
+        Hkv = rng.choice([1, 2, 4, 8])
+        cnts = [rng.choice([0, 0, 1, 2, 5, 16, 64, 129, 1000]) for _ in range(B)]
+        C = rng.choice([1, 2, 7, 64, 152])
+        m = Split(cnts, Hkv, C, rng.choice([0, 1, 4, 8, 256]))
+        if m.T == 0:
+            continue
+        for c in range(C + 1):
+            assert range_start_by_sequence(m, c) == m.range_start(c), (cnts, Hkv, C, m.W0, c)
