@@ -584,7 +584,6 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
     uint32_t *keys = reinterpret_cast<uint32_t *>(sc);
     constexpr int NT = Grp::warps * 32;
     constexpr int BPL = kSelBins / 32;   // histogram bins per lane of the scanning warp
-    static_assert(BPL == 32, "the digit search gives one bin of the holding lane to each lane");
     const int tid = grp.tid, lane = grp.lane(), warp = grp.warp();
     const int N = s.N, k = s.k;
     int32_t *selrow = p.selected + (size_t)u * p.max_budget;
@@ -663,28 +662,17 @@ __device__ void select_from_scores(const Grp &grp, const SelectParams &p, int u,
                     if (lane >= off) incl += t;
                 }
                 const int excl = incl - tot;
-                // the lane whose bins hold the wanted rank; its BPL = 32 bins,
-                // one per lane in descending digit order, are scanned by the
-                // whole warp and the first bin whose running count reaches
-                // `need` is the digit (a branch-free search, not a walk of 32
-                // dependent shared-memory reads)
-                const unsigned holder = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-                if (holder != 0u) {
-                    const int src = __ffs(holder) - 1;
-                    const int base = __shfl_sync(0xffffffffu, excl, src);
-                    const int bin = kSelBins - BPL * src - 1 - lane;
-                    const int c = x.hist[bin];
-                    int run = c;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const int t = __shfl_up_sync(0xffffffffu, run, off);
-                        if (lane >= off) run += t;
-                    }
-                    const unsigned reach = __ballot_sync(0xffffffffu, base + run >= need);
-                    if (lane == __ffs(reach) - 1) {
-                        x.digit = bin;
-                        x.above = base + run - c;
-                        x.cnt = c;
+                if (excl < need && need <= incl) {
+                    int run = excl;
+                    for (int j = 1; j <= BPL; ++j) {
+                        const int c = x.hist[top - j];
+                        if (run + c >= need) {
+                            x.digit = top - j;
+                            x.above = run;
+                            x.cnt = c;
+                            break;
+                        }
+                        run += c;
                     }
                 }
             }

@@ -4,11 +4,11 @@ select_from_scores), checked against a plain sort.
 The kernel finds tau, the key of the (k-2)-th best candidate, from 1024-bin
 histograms of 10-bit digits; in each pass one warp finds the bin holding the
 wanted rank: every lane sums 32 consecutive bins (descending digits), a warp
-scan over the lane totals names the holding lane, and that lane's 32 bins,
-one per lane, are scanned again to find the bin.  This file restates those
-steps in Python, with the lane arithmetic of the kernel, and checks that the
-two-level search agrees with a walk over the bins and that the selection it
-leads to is the top-k of a sort (ties to the lower page index).
+scan over the lane totals names the holding lane, and that lane walks its 32
+bins from the top.  This file restates those steps in Python, with the lane
+arithmetic of the kernel, and checks that the two-level search agrees with a
+walk over all bins and that the selection it leads to is the top-k of a sort
+(ties to the lower page index).
 
 The kept set is what "TinyServe: Query-Aware Cache Selection for Efficient
 LLM Serving", 方法详解 / 关键设计, asks for: the pages whose bounding-box
@@ -44,22 +44,22 @@ def digit_by_walk(hist, need):
     return None
 
 
-def digit_by_warp(hist, need):
-    """The same bin found as the kernel's warp does: lane totals, then the holding lane's bins."""
+def digit_by_lanes(hist, need):
+    """The same bin found as the kernel's warp does: lane totals and their scan
+    name the holding lane, which walks its own 32 bins."""
     tot = [sum(hist[BINS - BPL * (l + 1):BINS - BPL * l]) for l in range(LANES)]
     incl = list(np.cumsum(tot))
     excl = [incl[l] - tot[l] for l in range(LANES)]
-    holder = [l for l in range(LANES) if excl[l] < need <= incl[l]]
-    if not holder:
-        return None
-    src = holder[0]
-    base = excl[src]
-    bins = [BINS - BPL * src - 1 - lane for lane in range(LANES)]
-    c = [hist[b] for b in bins]
-    run = list(np.cumsum(c))
-    reach = [lane for lane in range(LANES) if base + run[lane] >= need]
-    j = reach[0]
-    return bins[j], base + run[j] - c[j], c[j]
+    for lane in range(LANES):
+        if excl[lane] < need <= incl[lane]:
+            top = BINS - BPL * lane
+            run = excl[lane]
+            for j in range(1, BPL + 1):
+                c = hist[top - j]
+                if run + c >= need:
+                    return top - j, run, c
+                run += c
+    return None
 
 
 def model_tau(cand_keys, kc, nt=128, passes=None):
@@ -79,7 +79,7 @@ def model_tau(cand_keys, kc, nt=128, passes=None):
         for key in cand_keys:
             if key & pmask == prefix:
                 hist[(key >> shift) & dmask] += 1
-        found = digit_by_warp(hist, need)
+        found = digit_by_lanes(hist, need)
         assert found == digit_by_walk(hist, need)
         digit, above, cnt = found
         need -= above
@@ -137,7 +137,7 @@ def sort_select(scores, k):
 
 
 @pytest.mark.parametrize("seed", range(6))
-def test_warp_search_matches_the_walk(seed):
+def test_lane_search_matches_the_walk(seed):
     rng = np.random.default_rng(seed)
     for _ in range(200):
         hist = [0] * BINS
@@ -146,18 +146,18 @@ def test_warp_search_matches_the_walk(seed):
             hist[int(b)] += int(rng.integers(1, 40))
         total = sum(hist)
         for need in {1, total, int(rng.integers(1, total + 1)), int(rng.integers(1, total + 1))}:
-            assert digit_by_warp(hist, need) == digit_by_walk(hist, need)
+            assert digit_by_lanes(hist, need) == digit_by_walk(hist, need)
 
 
-def test_warp_search_single_bin_and_lane_edges():
+def test_lane_search_single_bin_and_lane_edges():
     for b in (0, 31, 32, 511, 992, 1023):
         hist = [0] * BINS
         hist[b] = 5
         for need in (1, 3, 5):
-            assert digit_by_warp(hist, need) == (b, 0, 5)
+            assert digit_by_lanes(hist, need) == (b, 0, 5)
     hist = [1] * BINS
     for need in (1, 32, 33, 1000, 1024):
-        assert digit_by_warp(hist, need) == digit_by_walk(hist, need) == (BINS - need, need - 1, 1)
+        assert digit_by_lanes(hist, need) == digit_by_walk(hist, need) == (BINS - need, need - 1, 1)
 
 
 @pytest.mark.parametrize("kind", ["normal", "integers", "few_values", "signed"])
